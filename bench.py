@@ -1,0 +1,365 @@
+"""Benchmark: banded + global sparse attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 5] [--impl ours|reference]
+
+One step = one sa_forward call over one batch of the long-context workload
+(B=1, H=16, N=131072, D=128, window 1024, globals 0..63, bf16): gather of the
+global rows, band tiles, global-row split-K pass, merge.  The metric is useful
+(in-mask) attention FLOP/s: 4*D per scored (query, key) pair, pairs counted
+exactly by sa_count_pairs.  Inputs (1.6 GB) are larger than the 129 MB L2, so
+no flush is needed between steps.
+
+Prints ONE JSON line on rank 0.  Under torchrun each rank runs its own
+independent batch (weak scaling) and the time is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample of
+rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_long_context_banded_gb300 import inputs  # noqa: E402
+
+METRIC = "in-mask attention TFLOP/s & % of bf16 TC peak on 1 GB300 (N=4K–128K)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--oracle-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": p["bf16_tflops"], "bf16_tflops_sustained": p.get("bf16_tflops_sustained"),
+                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def workload_flops(w, sa):
+    """In-mask FLOPs per step: total and the band kernel's share (non-global rows)."""
+    per_head, total = sa.count_pairs(w.N, w.window, w.dilation, w.H, w.globals_)
+    pairs = w.B * total
+    global_pairs = w.B * w.H * len(w.globals_) * w.N
+    return 4.0 * w.D * pairs, 4.0 * w.D * (pairs - global_pairs), pairs
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("SA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file.read().splitlines() if ln.strip()]
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if len(r) > 1 and r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) > 2 and r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        loaded = [x for x in sm if x > 0.5 * (max(mx) if mx else 0)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def oracle_sample_timing(w, qkv, target_seconds: float, seed: int = 0):
+    """Time the fp64 oracle on a random sample of rows of the workload.
+
+    Returns (tflops, seconds, rows, threads).  The sample is uniform over all
+    B*H*N rows; its FLOPs are counted exactly from each sampled row's mask size.
+    """
+    import oracle
+    from sparse_long_context_banded_gb300 import sa
+
+    o = oracle.default()
+    threads = oracle.default_threads()
+    q, k, v = qkv
+    rng = np.random.default_rng(seed)
+    total_rows = w.B * w.H * w.N
+    # per-row mask sizes (exact): band length + globals outside it, or N for a global row
+    G = np.array(w.globals_, dtype=np.int64)
+
+    def row_pairs(rows):
+        i = rows % w.N
+        h = (rows // w.N) % w.H
+        d = np.array(w.dilation, dtype=np.int64)[h]
+        half = w.window // 2
+        lo = np.maximum(-half, -(i // d))
+        hi = np.minimum(half, (w.N - 1 - i) // d)
+        cnt = hi - lo + 1
+        for g in G:
+            diff = i - g
+            inside = (np.abs(diff) <= half * d) & (diff % d == 0)
+            cnt += (~inside).astype(np.int64)
+        is_g = np.isin(i, G)
+        cnt[is_g] = w.N
+        return cnt
+
+    n = 256
+    while True:
+        rows = np.sort(rng.choice(total_rows, size=min(n, total_rows), replace=False))
+        t0 = time.perf_counter()
+        o.forward_longformer(q, k, v, w.window, w.dilation, w.globals_, scale=w.scale,
+                             rows=rows, threads=threads, want_lse=False)
+        dt = time.perf_counter() - t0
+        if dt >= target_seconds or n >= total_rows:
+            break
+        n = int(min(total_rows, max(2 * n, n * target_seconds / max(dt, 1e-3) * 1.1)))
+    flops = 4.0 * w.D * float(row_pairs(rows).sum())
+    return flops / dt / 1e12, dt, int(rows.size), threads
+
+
+def run_reference(args):
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    w = inputs.workload(args.workload)
+    qkv = inputs.draw_qkv(w)
+    per_step = max(1.0, min(args.oracle_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    vals, secs = [], []
+    rows = threads = 0
+    for s in range(args.warmup + args.steps):
+        tf, dt, rows, threads = oracle_sample_timing(w, qkv, per_step, seed=s)
+        if s >= args.warmup:
+            vals.append(tf)
+            secs.append(dt)
+    value = statistics.median(vals)
+    sample = (f"{rows} uniformly drawn query rows of {w.B * w.H * w.N} per step "
+              f"(~{statistics.median(secs):.1f} s of fp64 CPU work)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "window": w.window, "n_globals": len(w.globals_)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+
+    from sparse_long_context_banded_gb300 import build, sa
+
+    rank, world = dist_setup()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    sa.load()
+
+    w = inputs.workload(args.workload)
+    # each rank runs its own independent batch of the workload (weak scaling)
+    qkv = inputs.draw_qkv(w, seed=(1000 + w.number) if rank == 0 else (1000 + w.number + 7919 * rank))
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def host_tensor(a):
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 \
+            else torch.from_numpy(a)
+        return t
+
+    hq, hk, hv = (host_tensor(a) for a in qkv)
+    q, k, v = (t.to(dev) for t in (hq, hk, hv))
+    out = torch.empty_like(q)
+    flops_step, band_flops, pairs = workload_flops(w, sa)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        sa.forward(q, k, v, w.window, w.dilation, w.globals_, scale=w.scale, out=out, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sa.sync_status(stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    sa.profile_begin()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prof = sa.profile_end()
+    barrier(world)
+    clocks = sampler.stop()
+    sa.sync_status(stream)
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    ms_step = ms_total / args.steps
+    value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+
+    pk = peaks()
+    band_ms = prof["band"]["ms"] / max(1, prof["band"]["launches"])
+    band_tflops = band_flops / (band_ms * 1e-3) / 1e12
+    launches = sum(p["launches"] for p in prof.values())
+
+    # end to end through the public call: pinned host inputs in, result back to host
+    e2e = None
+    if not args.no_e2e:
+        pq, pk_, pv = (t.pin_memory() for t in (hq, hk, hv))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        for _ in range(2):
+            q.copy_(pq, non_blocking=True)
+            k.copy_(pk_, non_blocking=True)
+            v.copy_(pv, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_steps = max(3, min(args.steps, 10))
+        barrier(world)
+        torch.cuda.synchronize()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(e2e_steps):
+            q.copy_(pq, non_blocking=True)
+            k.copy_(pk_, non_blocking=True)
+            v.copy_(pv, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+        x1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = max_over_ranks(x0.elapsed_time(x1), world, dev)
+        h2d = 3 * q.numel() * q.element_size()
+        d2h = out.numel() * out.element_size()
+        e2e = {"value": world * flops_step * e2e_steps / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": ms_e2e / e2e_steps, "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1:
+        tf, secs, rows, threads = oracle_sample_timing(w, qkv, args.oracle_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} uniformly drawn query rows of {w.B * w.H * w.N}, "
+                         f"{secs:.1f} s of fp64 CPU work"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if w.dtype == "bf16" else "fp32", "data": "synthetic",
+            "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                       "window": w.window, "n_globals": len(w.globals_),
+                       "in_mask_pairs_per_step": pairs * world,
+                       "in_mask_gflop_per_step": flops_step * world / 1e9,
+                       "l2": "inputs (1.6 GB) larger than L2; no flush",
+                       "pct_of_bf16_peak": 100.0 * value / (world * pk["bf16_tflops"])},
+            "roofline": {"bound": "tensor", "kernel": "band", "achieved": band_tflops,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": band_tflops / pk["bf16_tflops"], "traffic": None,
+                         "peak_source": f"{pk['source']} bf16 dense (burst)",
+                         "algorithmic_flops_per_launch": band_flops,
+                         "ms_per_launch": band_ms},
+            "stages_ms_per_step": {s: prof[s]["ms"] / max(1, prof[s]["launches"]) for s in prof},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+/*
+ * sa.h -- C ABI of the banded + global sparse attention library (forward).
+ *
+ * The operation (one attention head, query row i, key row j, positions 0..N-1):
+ *
+ *   S_i = { j : |i-j| <= floor(w/2)*d  and  (i-j) mod d == 0 }  U  G ,
+ *         and S_i = {0..N-1} when i is in G,
+ *   out[i] = sum_{j in S_i} softmax_j(scale * <q_i, k_j>) v_j .
+ *
+ * w is the window, d the head's dilation, G the set of global positions.
+ * Sources:
+ *  - Ultralytics glossary "Longformer", section "How the Longformer attention
+ *    works": a sliding window of w/2 positions on each side, a dilated window
+ *    with gaps of d between attended positions at the same cost, and global
+ *    tokens that attend to every position and are attended by every position.
+ *    The section's mask-count example fixes "within w/2" as the inclusive test
+ *    |i-j| <= w//2.
+ *  - "GMAT: Global Memory Augmentation for Transformers", sections
+ *    "Global-Memory Augmented Transformers" (sparse attention as an additive
+ *    {0,-inf} mask on Q K^T) and "Global Memory" (M memory tokens prefixed to
+ *    the sequence, dense in both directions).  GMAT memory is global_idx =
+ *    0..M-1 over the concatenated [memory; main] sequence: that mask is
+ *    identical to GMAT's main-sequence band plus dense memory rows/columns.
+ *  - "Unlimiformer", section 2.3, Eq. (1): softmax(Q K^T / sqrt(d_k)) V; the
+ *    caller passes scale (normally 1/sqrt(D)).
+ *
+ * Conventions for every entry point:
+ *  - Tensors are device pointers, contiguous [B, H, N, D] with D fastest,
+ *    16-byte aligned; the caller owns them.  q, k, v, out share one dtype.
+ *  - Host arrays (dilation, global_idx) are read during the call only; the
+ *    caller may free them on return.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream); the call returns once it is enqueued.  Launch failures return
+ *    SA_ERR_CUDA.  A kernel that detects a stalled wait records it in a
+ *    per-device error word that sa_sync_status() reports as SA_ERR_TIMEOUT.
+ *  - Validation happens before anything is launched; on any non-OK status
+ *    nothing was enqueued and sa_last_error() describes the problem.
+ *  - Thread safety: calls may come from several host threads and streams.
+ */
+#ifndef SA_H_
+#define SA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *sa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1, /* null pointer, bad size, index out of range      */
+  SA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. D not 64/128)   */
+  SA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed            */
+  SA_ERR_TIMEOUT = 4,     /* a kernel gave up on a stalled wait              */
+  SA_ERR_NO_MEMORY = 5    /* device scratch could not be allocated           */
+} sa_status;
+
+typedef enum { SA_BF16 = 0, SA_FP32 = 1 } sa_dtype;
+
+/* Largest number of distinct global positions accepted. */
+#define SA_MAX_GLOBALS 256
+
+/*
+ * sa_forward -- out = banded + global sparse attention of (q, k, v).
+ *
+ *  q, k, v   device, [B,H,N,D] in `dtype`; read only.
+ *  out       device, [B,H,N,D] in `dtype`; fully written.
+ *  B, H, N   >= 1.   D: 64 or 128 (else SA_ERR_UNSUPPORTED).
+ *  window    w >= 0; half-width floor(w/2).
+ *  dilation  host, H entries >= 1 (per head), or NULL for all 1.
+ *  global_idx host, n_global entries in [0, N); duplicates are merged (a set).
+ *            May be NULL when n_global == 0.  At most SA_MAX_GLOBALS distinct.
+ *  scale     multiplier of q.k before the softmax (finite).
+ *  dtype     SA_BF16 (tensor-core path, fp32 accumulation and softmax, bf16
+ *            output) or SA_FP32 (fp32 arithmetic throughout, fp32 output).
+ *  stream    cudaStream_t on which all work is enqueued.
+ *
+ * Device scratch (gathered global rows, split-K partials) comes from a
+ * library-owned stream-ordered pool; exhaustion returns SA_ERR_NO_MEMORY.
+ */
+sa_status sa_forward(const void *q, const void *k, const void *v, void *out, int B,
+                     int H, int N, int D, int window, const int32_t *dilation,
+                     const int32_t *global_idx, int n_global, float scale,
+                     sa_dtype dtype, sa_stream_t stream);
+
+/*
+ * sa_forward_lse -- sa_forward, and also the natural-log log-sum-exp of each
+ * row's masked scores: lse[b,h,i] = log(sum_{j in S_i} exp(scale*<q_i,k_j>)).
+ *  lse   device, [B,H,N] float32, or NULL (then identical to sa_forward).
+ */
+sa_status sa_forward_lse(const void *q, const void *k, const void *v, void *out,
+                         float *lse, int B, int H, int N, int D, int window,
+                         const int32_t *dilation, const int32_t *global_idx,
+                         int n_global, float scale, sa_dtype dtype,
+                         sa_stream_t stream);
+
+/*
+ * sa_count_pairs -- exact number of (i, j) pairs in the mask, |S_i| summed
+ * over i, per head (per_head[H], may be NULL) and over all heads of one batch
+ * element (*total, may be NULL).  Host only, integer arithmetic, no GPU use.
+ * Same arguments and validation as sa_forward.  The in-mask FLOP count of a
+ * call is 4 * D * B * total (2D for q.k and 2D for p*v per pair).
+ */
+sa_status sa_count_pairs(int N, int window, const int32_t *dilation, int H,
+                         const int32_t *global_idx, int n_global, int64_t *per_head,
+                         int64_t *total);
+
+/* Thread-local description of the last non-OK status on this host thread. */
+const char *sa_last_error(void);
+
+/*
+ * sa_sync_status -- waits for `stream`, then reports (and clears) the current
+ * device's error word: SA_ERR_TIMEOUT if a kernel gave up on a stalled wait,
+ * SA_ERR_CUDA if the stream reported an error, else SA_OK.
+ */
+sa_status sa_sync_status(sa_stream_t stream);
+
+/*
+ * Per-stage timing.  Between sa_profile_begin() and sa_profile_end(), every
+ * sa_forward* call records CUDA events around each of its kernel launches on
+ * its own stream.  sa_profile_end() waits for those events and returns, per
+ * stage, the number of launches and their summed device time in milliseconds.
+ * Stages: 0 gather of global rows, 1 band tiles, 2 global-row split-K pass,
+ * 3 merge of partial softmax statistics.  Process-wide; not for concurrent use
+ * from several threads.
+ */
+#define SA_NUM_STAGES 4
+typedef struct {
+  int64_t launches[SA_NUM_STAGES];
+  double ms[SA_NUM_STAGES];
+} sa_profile;
+
+sa_status sa_profile_begin(void);
+sa_status sa_profile_end(sa_profile *out);
+
+/* Library version string. */
+const char *sa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_H_ */

@@ -1,0 +1,448 @@
+// sa_api.cu -- the C ABI: argument checks, schedule cache, scratch, launches.
+//
+// One sa_forward call enqueues, on the caller's stream:
+//   1. gather    -- q/k/v rows of the global positions into compact buffers
+//   2. band      -- per query tile: the key tiles of its band, then the global
+//                   key tile(s); writes every row of `out` (global rows too)
+//   3. global    -- the global rows against all N keys, split over key chunks,
+//                   each CTA leaving a partial (max, sum, unnormalised output)
+//   4. merge     -- combines the partials and overwrites the global rows
+// Steps 1, 3 and 4 run only when the global set is not empty.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "sa.h"
+#include "sa_internal.h"
+#include "sa_kernels.h"
+#include "sa_tc.h"
+
+namespace sa {
+namespace {
+
+thread_local std::string t_last_error;
+
+sa_status fail(sa_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+sa_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(SA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------------------
+// per-device state: error word, scratch pool, cached schedules
+
+struct DeviceSchedule {
+  Schedule host;
+  Slot *slots = nullptr;
+  BandItem *band = nullptr;
+  GlobalItem *global = nullptr;
+  int32_t *globals = nullptr;
+};
+
+struct DeviceState {
+  int *err = nullptr;
+  cudaMemPool_t pool = nullptr;
+  std::map<std::string, std::unique_ptr<DeviceSchedule>> schedules;
+};
+
+std::mutex g_mutex;
+std::map<int, std::unique_ptr<DeviceState>> g_devices;
+constexpr size_t kMaxCachedSchedules = 256;
+
+sa_status device_state(int dev, DeviceState **out) {
+  auto it = g_devices.find(dev);
+  if (it != g_devices.end()) {
+    *out = it->second.get();
+    return SA_OK;
+  }
+  auto ds = std::make_unique<DeviceState>();
+  cudaError_t e = cudaMalloc(&ds->err, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+  e = cudaMemset(ds->err, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+  cudaMemPoolProps props{};
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  e = cudaMemPoolCreate(&ds->pool, &props);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+  uint64_t keep = ~0ull;  // keep freed scratch in the pool between calls
+  cudaMemPoolSetAttribute(ds->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  *out = ds.get();
+  g_devices[dev] = std::move(ds);
+  return SA_OK;
+}
+
+template <typename X>
+sa_status upload(const std::vector<X> &v, X **dst) {
+  *dst = nullptr;
+  if (v.empty()) return SA_OK;
+  cudaError_t e = cudaMalloc(dst, sizeof(X) * v.size());
+  if (e != cudaSuccess) return fail(SA_ERR_NO_MEMORY, "cudaMalloc(schedule): %s", cudaGetErrorString(e));
+  e = cudaMemcpy(*dst, v.data(), sizeof(X) * v.size(), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(schedule)");
+  return SA_OK;
+}
+
+void free_schedule(DeviceSchedule &s) {
+  cudaFree(s.slots);
+  cudaFree(s.band);
+  cudaFree(s.global);
+  cudaFree(s.globals);
+}
+
+std::string schedule_key(const Problem &p, int family) {
+  std::string k;
+  auto put = [&k](const void *x, size_t n) { k.append(static_cast<const char *>(x), n); };
+  int head[7] = {family, p.B, p.H, p.N, p.D, p.window, (int)p.globals.size()};
+  put(head, sizeof head);
+  put(p.dilation.data(), sizeof(int32_t) * p.dilation.size());
+  put(p.globals.data(), sizeof(int32_t) * p.globals.size());
+  return k;
+}
+
+// Schedules are immutable once uploaded, so calls on any stream may share them.
+sa_status get_schedule(DeviceState &ds, const Problem &p, int family, const Tiling &t,
+                       const DeviceSchedule **out) {
+  const std::string key = schedule_key(p, family);
+  auto it = ds.schedules.find(key);
+  if (it != ds.schedules.end()) {
+    *out = it->second.get();
+    return SA_OK;
+  }
+  if (ds.schedules.size() >= kMaxCachedSchedules) {
+    cudaDeviceSynchronize();  // nothing may still read the evicted schedules
+    for (auto &kv : ds.schedules) free_schedule(*kv.second);
+    ds.schedules.clear();
+  }
+  auto s = std::make_unique<DeviceSchedule>();
+  s->host = build_schedule(p, t);
+  sa_status st;
+  if ((st = upload(s->host.slots, &s->slots)) != SA_OK ||
+      (st = upload(s->host.band, &s->band)) != SA_OK ||
+      (st = upload(s->host.global, &s->global)) != SA_OK ||
+      (st = upload(p.globals, &s->globals)) != SA_OK) {
+    free_schedule(*s);
+    return st;
+  }
+  *out = s.get();
+  ds.schedules[key] = std::move(s);
+  return SA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// profiling events
+
+struct ProfileRecord {
+  int stage;
+  cudaEvent_t start, stop;
+};
+struct Profiler {
+  bool on = false;
+  std::vector<ProfileRecord> records;
+  std::vector<cudaEvent_t> spare;
+  cudaEvent_t get() {
+    if (!spare.empty()) {
+      cudaEvent_t e = spare.back();
+      spare.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+} g_prof;
+
+struct StageTimer {
+  int stage;
+  cudaStream_t stream;
+  cudaEvent_t start = nullptr;
+  StageTimer(int s, cudaStream_t st) : stage(s), stream(st) {
+    if (g_prof.on) {
+      start = g_prof.get();
+      cudaEventRecord(start, stream);
+    }
+  }
+  void done() {
+    if (start) {
+      cudaEvent_t stop = g_prof.get();
+      cudaEventRecord(stop, stream);
+      g_prof.records.push_back({stage, start, stop});
+      start = nullptr;
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+
+sa_status forward_impl(const void *q, const void *k, const void *v, void *out, float *lse,
+                       int B, int H, int N, int D, int window, const int32_t *dilation,
+                       const int32_t *global_idx, int n_global, float scale, sa_dtype dtype,
+                       cudaStream_t stream) {
+  if (!q || !k || !v || !out) return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be non-null");
+  if (n_global < 0) return fail(SA_ERR_INVALID_ARG, "n_global must be >= 0");
+  if (n_global > 0 && !global_idx)
+    return fail(SA_ERR_INVALID_ARG, "global_idx is null but n_global = %d", n_global);
+  if (H < 1) return fail(SA_ERR_INVALID_ARG, "H must be >= 1 (got %d)", H);
+  const void *ptrs[4] = {q, k, v, out};
+  for (int i = 0; i < 4; ++i)
+    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0)
+      return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0)
+    return fail(SA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+
+  Problem p;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.D = D;
+  p.window = window;
+  p.half = window / 2;
+  if (dilation)
+    p.dilation.assign(dilation, dilation + H);
+  else
+    p.dilation.assign(H, 1);
+  p.scale = scale;
+  p.dtype = dtype;
+  for (int i = 0; i < n_global; ++i)
+    if (global_idx[i] < 0 || global_idx[i] >= N)
+      return fail(SA_ERR_INVALID_ARG, "global_idx[%d] = %d outside [0, %d)", i, global_idx[i], N);
+  p.globals = global_set(global_idx, n_global);
+  std::string why = validate(p);
+  if (!why.empty()) return fail(SA_ERR_INVALID_ARG, "%s", why.c_str());
+  if (D != 64 && D != 128) return fail(SA_ERR_UNSUPPORTED, "D = %d (supported: 64, 128)", D);
+  if ((int)p.globals.size() > SA_MAX_GLOBALS)
+    return fail(SA_ERR_UNSUPPORTED, "%d distinct globals (at most %d)", (int)p.globals.size(),
+                SA_MAX_GLOBALS);
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState *ds = nullptr;
+  sa_status st = device_state(dev, &ds);
+  if (st != SA_OK) return st;
+
+  const bool tc = (dtype == SA_BF16);
+  const Tiling tiling = tc ? tc_tiling(D) : kSimtTiling;
+  const DeviceSchedule *sched = nullptr;
+  st = get_schedule(*ds, p, tc ? 1 : 0, tiling, &sched);
+  if (st != SA_OK) return st;
+  const Schedule &hs = sched->host;
+
+  DevProblem dp{};
+  dp.q = q;
+  dp.k = k;
+  dp.v = v;
+  dp.out = out;
+  dp.lse = lse;
+  dp.N = N;
+  dp.D = D;
+  dp.H = H;
+  dp.half = p.half;
+  dp.scale_log2 = scale * 1.4426950408889634f;
+  dp.globals = sched->globals;
+  dp.n_g = (int)p.globals.size();
+  dp.g_pad = hs.g_pad;
+  dp.slots = sched->slots;
+  dp.band = sched->band;
+  dp.n_band = (int)hs.band.size();
+  dp.gitems = sched->global;
+  dp.n_gitems = (int)hs.global.size();
+  dp.n_chunks = hs.n_chunks;
+  dp.chunk_len = hs.chunk_len;
+  dp.err = ds->err;
+
+  const int BH = B * H;
+  const size_t esize = dtype == SA_BF16 ? 2 : 4;
+  const size_t g_rows = (size_t)BH * hs.g_pad * D;
+  const size_t part_rows = (size_t)BH * hs.n_chunks * hs.g_pad;
+  size_t off_q = 0, off_k = 0, off_v = 0, off_po = 0, off_ml = 0, total = 0;
+  auto carve = [&total](size_t bytes) {
+    size_t at = total;
+    total += (bytes + 255) & ~size_t(255);
+    return at;
+  };
+  if (dp.n_g > 0) {
+    off_q = carve(g_rows * esize);
+    off_k = carve(g_rows * esize);
+    off_v = carve(g_rows * esize);
+    off_po = carve(part_rows * D * sizeof(float));
+    off_ml = carve(part_rows * 2 * sizeof(float));
+  }
+  char *scratch = nullptr;
+  if (total > 0) {
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&scratch), total, ds->pool, stream);
+    if (e != cudaSuccess)
+      return fail(SA_ERR_NO_MEMORY, "scratch of %zu bytes: %s", total, cudaGetErrorString(e));
+    dp.qg = scratch + off_q;
+    dp.kg = scratch + off_k;
+    dp.vg = scratch + off_v;
+    dp.part_o = reinterpret_cast<float *>(scratch + off_po);
+    dp.part_ml = reinterpret_cast<float *>(scratch + off_ml);
+  }
+
+  sa_status result = SA_OK;
+  auto step = [&](int stage, auto &&launch, const char *what) {
+    if (result != SA_OK) return;
+    StageTimer timer(stage, stream);
+    cudaError_t le = launch();
+    timer.done();
+    if (le != cudaSuccess) result = cuda_fail(le, what);
+  };
+  if (dp.n_g > 0) step(0, [&] { return launch_gather(dp, BH, dtype, stream); }, "gather launch");
+  if (tc)
+    step(1, [&] { return launch_band_tc(dp, stream); }, "band (tensor-core) launch");
+  else
+    step(1, [&] { return launch_band_simt(dp, dtype, stream); }, "band launch");
+  if (dp.n_g > 0) {
+    if (tc)
+      step(2, [&] { return launch_global_tc(dp, stream); }, "global-row (tensor-core) launch");
+    else
+      step(2, [&] { return launch_global_simt(dp, dtype, stream); }, "global-row launch");
+    step(3, [&] { return launch_merge(dp, BH, dtype, stream); }, "merge launch");
+  }
+  if (scratch) {
+    e = cudaFreeAsync(scratch, stream);
+    if (e != cudaSuccess && result == SA_OK) result = cuda_fail(e, "cudaFreeAsync(scratch)");
+  }
+  return result;
+}
+
+}  // namespace
+}  // namespace sa
+
+using namespace sa;
+
+extern "C" sa_status sa_forward(const void *q, const void *k, const void *v, void *out, int B,
+                                int H, int N, int D, int window, const int32_t *dilation,
+                                const int32_t *global_idx, int n_global, float scale,
+                                sa_dtype dtype, sa_stream_t stream) {
+  return forward_impl(q, k, v, out, nullptr, B, H, N, D, window, dilation, global_idx,
+                      n_global, scale, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" sa_status sa_forward_lse(const void *q, const void *k, const void *v, void *out,
+                                    float *lse, int B, int H, int N, int D, int window,
+                                    const int32_t *dilation, const int32_t *global_idx,
+                                    int n_global, float scale, sa_dtype dtype,
+                                    sa_stream_t stream) {
+  return forward_impl(q, k, v, out, lse, B, H, N, D, window, dilation, global_idx, n_global,
+                      scale, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" sa_status sa_count_pairs(int N, int window, const int32_t *dilation, int H,
+                                    const int32_t *global_idx, int n_global, int64_t *per_head,
+                                    int64_t *total) {
+  if (n_global < 0) return fail(SA_ERR_INVALID_ARG, "n_global must be >= 0");
+  if (n_global > 0 && !global_idx)
+    return fail(SA_ERR_INVALID_ARG, "global_idx is null but n_global = %d", n_global);
+  if (H < 1) return fail(SA_ERR_INVALID_ARG, "H must be >= 1 (got %d)", H);
+  Problem p;
+  p.B = 1;
+  p.H = H;
+  p.N = N;
+  p.D = 64;
+  p.window = window;
+  p.half = window / 2;
+  if (dilation)
+    p.dilation.assign(dilation, dilation + H);
+  else
+    p.dilation.assign(H, 1);
+  p.scale = 1.f;
+  p.dtype = SA_BF16;
+  for (int i = 0; i < n_global; ++i)
+    if (global_idx[i] < 0 || global_idx[i] >= N)
+      return fail(SA_ERR_INVALID_ARG, "global_idx[%d] = %d outside [0, %d)", i, global_idx[i], N);
+  p.globals = global_set(global_idx, n_global);
+  std::string why = validate(p);
+  if (!why.empty()) return fail(SA_ERR_INVALID_ARG, "%s", why.c_str());
+  if ((int)p.globals.size() > SA_MAX_GLOBALS)
+    return fail(SA_ERR_UNSUPPORTED, "%d distinct globals (at most %d)", (int)p.globals.size(),
+                SA_MAX_GLOBALS);
+  int64_t sum = 0;
+  for (int h = 0; h < H; ++h) {
+    const int64_t c = pairs_of_head(N, p.half, p.dilation[h], p.globals);
+    if (per_head) per_head[h] = c;
+    sum += c;
+  }
+  if (total) *total = sum;
+  return SA_OK;
+}
+
+extern "C" const char *sa_last_error(void) { return t_last_error.c_str(); }
+
+extern "C" sa_status sa_sync_status(sa_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int *word = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_devices.find(dev);
+    if (it == g_devices.end()) return SA_OK;  // nothing ever ran here
+    word = it->second->err;
+  }
+  int h = 0;
+  e = cudaMemcpy(&h, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (h != 0) {
+    cudaMemset(word, 0, sizeof(int));
+    if (h & kErrWaitTimeout)
+      return fail(SA_ERR_TIMEOUT, "a kernel gave up on a stalled wait (error word 0x%x)", h);
+    return fail(SA_ERR_CUDA, "a kernel failed a device-side check (error word 0x%x)", h);
+  }
+  return SA_OK;
+}
+
+extern "C" sa_status sa_profile_begin(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  for (auto &r : g_prof.records) {
+    g_prof.spare.push_back(r.start);
+    g_prof.spare.push_back(r.stop);
+  }
+  g_prof.records.clear();
+  g_prof.on = true;
+  return SA_OK;
+}
+
+extern "C" sa_status sa_profile_end(sa_profile *out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_prof.on = false;
+  sa_profile res{};
+  sa_status st = SA_OK;
+  for (auto &r : g_prof.records) {
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e != cudaSuccess && st == SA_OK) st = cuda_fail(e, "profile event");
+    res.launches[r.stage] += 1;
+    res.ms[r.stage] += ms;
+    g_prof.spare.push_back(r.start);
+    g_prof.spare.push_back(r.stop);
+  }
+  g_prof.records.clear();
+  if (out) *out = res;
+  return st;
+}
+
+extern "C" const char *sa_version(void) { return "sa-gb300 0.1 (sm_103a)"; }

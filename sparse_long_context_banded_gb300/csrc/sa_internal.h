@@ -1,0 +1,81 @@
+// sa_internal.h -- structures shared by the host scheduler and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "sa.h"
+
+namespace sa {
+
+// One residue class of one dilation value: positions r, r+d, r+2d, ... (< N).
+// A dilated band |i-j| <= half*d, d | (i-j) is an ordinary band of half-width
+// `half` on each class, so every kernel works in class coordinates t, with
+// position = r + d*t and t in [0, len).
+struct Slot {
+  int32_t d;
+  int32_t r;
+  int32_t len;  // ceil((N - r) / d)
+  int32_t pad;
+};
+
+// One CTA of band work: query tiles q_tile, q_tile+1, ... (nq of them, class
+// coordinates, `rows` rows each) of head bh in residue class `slot`.  For query
+// tile u the key tiles k_lo[u]..k_hi[u] (inclusive, `key_tile` keys each)
+// intersect the band; flags bit u says whether any global key falls inside
+// that query tile's band reach (so the global tile must drop duplicates).
+struct BandItem {
+  int32_t bh;
+  int32_t slot;
+  int32_t q_tile;
+  int32_t flags;
+  int32_t k_lo[2];
+  int32_t k_hi[2];
+};
+
+// One CTA of the global-row pass: head bh, key chunk `chunk` (keys
+// [chunk*chunk_len, min(N, (chunk+1)*chunk_len))), global-row tile `g_tile`.
+struct GlobalItem {
+  int32_t bh;
+  int32_t chunk;
+  int32_t g_tile;
+  int32_t pad;
+};
+
+// Host-side description of one call.
+struct Problem {
+  int B, H, N, D;
+  int window, half;
+  std::vector<int32_t> dilation;  // per head
+  std::vector<int32_t> globals;   // sorted, unique
+  float scale;
+  sa_dtype dtype;
+};
+
+// Tiling of one kernel family.
+struct Tiling {
+  int rows;        // query rows per tile
+  int q_tiles;     // query tiles per CTA (1 or 2)
+  int key_tile;    // keys per band tile
+  int g_tile;      // keys per global tile (and global query rows per tile)
+  int target_ctas; // CTAs wanted for the global-row pass
+};
+
+// Full launch schedule of one problem for one tiling.
+struct Schedule {
+  std::vector<Slot> slots;
+  std::vector<int32_t> head_slot0;  // first slot index of each head's dilation
+  std::vector<BandItem> band;
+  std::vector<GlobalItem> global;
+  int n_chunks = 0, chunk_len = 0, g_pad = 0;
+  int64_t band_tile_pairs = 0;  // executed (query tile, key tile) pairs
+};
+
+// Host scheduler (sa_schedule.cpp).
+std::string validate(const Problem &p);
+std::vector<int32_t> global_set(const int32_t *idx, int n);
+Schedule build_schedule(const Problem &p, const Tiling &t);
+int64_t pairs_of_head(int N, int half, int d, const std::vector<int32_t> &globals);
+
+}  // namespace sa

@@ -1,0 +1,47 @@
+// sa_kernels.h -- device-side view of one call, and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "sa_internal.h"
+
+namespace sa {
+
+// Error bits OR-ed into the per-device error word by kernels.
+enum : int {
+  kErrWaitTimeout = 1,  // an mbarrier wait gave up (bounded spin ran out)
+  kErrBadWork = 2,      // a work item failed a device-side range check
+};
+
+struct DevProblem {
+  const void *q, *k, *v;
+  void *out;
+  float *lse;       // [B*H*N] or null
+  int N, D, H;
+  int half;         // floor(window / 2)
+  float scale_log2; // scale * log2(e): scores are kept in base-2 units
+  const int32_t *globals;  // device, sorted unique, n_g entries
+  int n_g, g_pad;
+  const Slot *slots;
+  const BandItem *band;
+  int n_band;
+  const GlobalItem *gitems;
+  int n_gitems;
+  int n_chunks, chunk_len;
+  // scratch
+  void *qg, *kg, *vg;  // [B*H][g_pad][D] gathered global rows, input dtype
+  float *part_o;       // [B*H][n_chunks][g_pad][D]  unnormalised partial outputs
+  float *part_ml;      // [B*H][n_chunks][g_pad][2]  partial (max, sum), base 2
+  int *err;
+};
+
+// SIMT path (fp32 inputs): CUDA-core arithmetic, fp32 throughout.
+constexpr Tiling kSimtTiling{64, 1, 64, 64, 608};
+cudaError_t launch_gather(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s);
+cudaError_t launch_band_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s);
+cudaError_t launch_global_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s);
+cudaError_t launch_merge(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s);
+
+}  // namespace sa

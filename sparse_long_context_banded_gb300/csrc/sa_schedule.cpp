@@ -1,0 +1,182 @@
+// sa_schedule.cpp -- argument checks, the global index set, the band-tile
+// schedule and the exact in-mask pair count.  Host code, integer arithmetic.
+//
+// Mask (Ultralytics glossary "Longformer", section "How the Longformer
+// attention works"): row i scores key j when |i-j| <= floor(w/2)*d and d
+// divides i-j (the dilated sliding window; d = 1 is the plain window), and
+// every row scores every global key while a global row scores every key.
+// Global positions form a set: listing one twice changes nothing, as the
+// section's mask-count example assigns True to a global row and column.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <numeric>
+
+#include "sa_internal.h"
+
+namespace sa {
+
+std::string validate(const Problem &p) {
+  char buf[256];
+  if (p.B < 1 || p.H < 1 || p.N < 1) {
+    snprintf(buf, sizeof buf, "B, H, N must be >= 1 (got %d, %d, %d)", p.B, p.H, p.N);
+    return buf;
+  }
+  if (p.window < 0) {
+    snprintf(buf, sizeof buf, "window must be >= 0 (got %d)", p.window);
+    return buf;
+  }
+  if ((int)p.dilation.size() != p.H) return "dilation must have H entries";
+  for (int h = 0; h < p.H; ++h)
+    if (p.dilation[h] < 1) {
+      snprintf(buf, sizeof buf, "dilation[%d] = %d must be >= 1", h, p.dilation[h]);
+      return buf;
+    }
+  for (int32_t g : p.globals)
+    if (g < 0 || g >= p.N) {
+      snprintf(buf, sizeof buf, "global index %d outside [0, %d)", g, p.N);
+      return buf;
+    }
+  if (!std::isfinite(p.scale)) return "scale must be finite";
+  if (p.dtype != SA_BF16 && p.dtype != SA_FP32) return "unknown dtype";
+  const double elems = (double)p.B * p.H * p.N * std::max(p.D, 1);
+  if (elems > 9.0e18) return "tensor too large";
+  return "";
+}
+
+std::vector<int32_t> global_set(const int32_t *idx, int n) {
+  std::vector<int32_t> g(idx, idx + std::max(n, 0));
+  std::sort(g.begin(), g.end());
+  g.erase(std::unique(g.begin(), g.end()), g.end());
+  return g;
+}
+
+// Number of t with |t| <= half and 0 <= i + t*d < N.
+static inline int64_t band_len(int64_t N, int64_t half, int64_t d, int64_t i) {
+  const int64_t lo = std::max(-half, -(i / d));
+  const int64_t hi = std::min(half, (N - 1 - i) / d);
+  return hi - lo + 1;
+}
+
+static inline bool in_band(int64_t half, int64_t d, int64_t i, int64_t j) {
+  const int64_t diff = i - j;
+  return (diff <= half * d && -diff <= half * d) && (diff % d == 0);
+}
+
+// |mask| of one head:
+//   sum over non-global rows of (band length + globals outside the band)
+//   + N per global row.
+// The globals-inside-band term is counted from the globals' side (the band
+// relation is symmetric), so the cost is O(N + |G|^2).
+int64_t pairs_of_head(int N, int half, int d, const std::vector<int32_t> &G) {
+  const int64_t n_g = (int64_t)G.size();
+  int64_t band_all = 0;
+  for (int64_t i = 0; i < N; ++i) band_all += band_len(N, half, d, i);
+  int64_t band_g = 0;            // band lengths of the global rows
+  int64_t g_in_band_of_g = 0;    // pairs (g, g') of globals inside each other's band
+  for (int32_t g : G) {
+    band_g += band_len(N, half, d, g);
+    for (int32_t g2 : G) g_in_band_of_g += in_band(half, d, g, g2) ? 1 : 0;
+  }
+  // non-global rows i: band_len(i) + n_g - |{g in band(i)}|
+  // sum_{i not in G} |{g in band(i)}| = sum_g (band_len(g) - |{i in G in band(g)}|)
+  const int64_t rows_ng = (int64_t)N - n_g;
+  const int64_t g_in_band_rows = band_g - g_in_band_of_g;
+  return (band_all - band_g) + rows_ng * n_g - g_in_band_rows + n_g * (int64_t)N;
+}
+
+Schedule build_schedule(const Problem &p, const Tiling &t) {
+  Schedule s;
+  const int64_t half = p.half;
+  // residue-class slots, one group per distinct dilation value
+  std::vector<int32_t> dvals(p.dilation);
+  std::sort(dvals.begin(), dvals.end());
+  dvals.erase(std::unique(dvals.begin(), dvals.end()), dvals.end());
+  std::vector<int32_t> first_slot(dvals.size());
+  for (size_t a = 0; a < dvals.size(); ++a) {
+    first_slot[a] = (int32_t)s.slots.size();
+    const int d = dvals[a];
+    for (int r = 0; r < d && r < p.N; ++r)
+      s.slots.push_back(Slot{d, r, (int32_t)((p.N - r + d - 1) / d), 0});
+  }
+  s.head_slot0.resize(p.H);
+  for (int h = 0; h < p.H; ++h) {
+    const size_t a = std::lower_bound(dvals.begin(), dvals.end(), p.dilation[h]) - dvals.begin();
+    s.head_slot0[h] = first_slot[a];
+  }
+
+  // band work: every query tile of every residue class of every head, with the
+  // key tiles that intersect its band
+  const int n_g = (int)p.globals.size();
+  std::vector<std::pair<int, BandItem>> items;
+  for (int b = 0; b < p.B; ++b)
+    for (int h = 0; h < p.H; ++h) {
+      const int d = p.dilation[h];
+      for (int r = 0; r < d && r < p.N; ++r) {
+        const int slot = s.head_slot0[h] + r;
+        const int64_t len = s.slots[slot].len;
+        const int64_t n_tiles = (len + t.rows - 1) / t.rows;
+        for (int64_t t0 = 0; t0 < n_tiles; t0 += t.q_tiles) {
+          BandItem it{};
+          it.bh = b * p.H + h;
+          it.slot = slot;
+          it.q_tile = (int32_t)t0;
+          int work = 0;
+          for (int u = 0; u < 2; ++u) {
+            const int64_t tt = t0 + u;
+            if (u >= t.q_tiles || tt >= n_tiles) {
+              it.k_lo[u] = 0;
+              it.k_hi[u] = -1;
+              continue;
+            }
+            const int64_t row_lo = tt * t.rows;
+            const int64_t row_hi = std::min(len - 1, row_lo + t.rows - 1);
+            const int64_t key_lo = std::max<int64_t>(0, row_lo - half);
+            const int64_t key_hi = std::min<int64_t>(len - 1, row_hi + half);
+            it.k_lo[u] = (int32_t)(key_lo / t.key_tile);
+            it.k_hi[u] = (int32_t)(key_hi / t.key_tile);
+            work += it.k_hi[u] - it.k_lo[u] + 1;
+            s.band_tile_pairs += it.k_hi[u] - it.k_lo[u] + 1;
+            // does a global key of this class fall inside the band reach?
+            for (int32_t g : p.globals) {
+              if ((g - r) % d != 0) continue;
+              const int64_t tg = (g - r) / d;
+              if (tg >= row_lo - half && tg <= row_hi + half) {
+                it.flags |= 1 << u;
+                break;
+              }
+            }
+          }
+          items.push_back({work, it});
+        }
+      }
+    }
+  // longest work first (stable, so equal-work items keep their sequence order
+  // and neighbouring CTAs keep sharing key/value tiles in L2)
+  std::stable_sort(items.begin(), items.end(),
+                   [](const std::pair<int, BandItem> &a, const std::pair<int, BandItem> &b) {
+                     return a.first > b.first;
+                   });
+  s.band.reserve(items.size());
+  for (auto &x : items) s.band.push_back(x.second);
+
+  // global-row pass: split the N keys into chunks so that enough CTAs run
+  if (n_g > 0) {
+    const int g_tiles = (n_g + t.g_tile - 1) / t.g_tile;
+    s.g_pad = g_tiles * t.g_tile;
+    const int64_t bh = (int64_t)p.B * p.H;
+    const int64_t max_chunks = (p.N + t.key_tile - 1) / t.key_tile;
+    int64_t want = (t.target_ctas + bh * g_tiles - 1) / (bh * g_tiles);
+    want = std::max<int64_t>(1, std::min(want, max_chunks));
+    const int64_t per = (p.N + want - 1) / want;
+    s.chunk_len = (int)(((per + t.key_tile - 1) / t.key_tile) * t.key_tile);
+    s.n_chunks = (int)((p.N + s.chunk_len - 1) / s.chunk_len);
+    for (int64_t x = 0; x < bh; ++x)
+      for (int c = 0; c < s.n_chunks; ++c)
+        for (int gt = 0; gt < g_tiles; ++gt)
+          s.global.push_back(GlobalItem{(int32_t)x, c, gt, 0});
+  }
+  return s;
+}
+
+}  // namespace sa

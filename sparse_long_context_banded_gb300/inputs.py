@@ -87,10 +87,18 @@ def custom(B: int, H: int, N: int, D: int, window: int, dilation: Sequence[int] 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bfloat16 bit patterns (uint16), round to nearest, ties to even."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32)
-    rounding = ((u >> 16) & 1) + np.uint32(0x7FFF)
-    return ((u + rounding) >> 16).astype(np.uint16)
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).reshape(-1)
+    out = np.empty(u.shape, dtype=np.uint16)
+    step = 1 << 20
+    for s in range(0, u.size, step):
+        uc = u[s:s + step]
+        r = uc >> np.uint32(16)
+        r &= np.uint32(1)
+        r += np.uint32(0x7FFF)
+        r += uc
+        r >>= np.uint32(16)
+        out[s:s + step] = r
+    return out.reshape(np.shape(x))
 
 
 def bf16_bits_to_float32(bits: np.ndarray) -> np.ndarray:

@@ -1,0 +1,167 @@
+"""ctypes binding of the C ABI in ``include/sa.h`` (argument marshalling only).
+
+Every step of the attention runs in the CUDA library; this module passes
+pointers, sizes and the current CUDA stream.  It raises ``SaError`` for any
+non-OK status and ``RuntimeError`` if the compiled library is missing -- there
+is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+from . import build as _build
+
+SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_TIMEOUT, SA_ERR_NO_MEMORY = range(6)
+SA_BF16, SA_FP32 = 0, 1
+SA_MAX_GLOBALS = 256
+STAGES = ("gather", "band", "global_rows", "merge")
+
+STATUS_NAMES = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_ERR_CUDA",
+                4: "SA_ERR_TIMEOUT", 5: "SA_ERR_NO_MEMORY"}
+
+# Every function include/sa.h declares, with its ctypes signature.
+_VP, _I, _F, _I32P, _I64P = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p
+
+
+class _Profile(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int64 * 4), ("ms", ctypes.c_double * 4)]
+
+
+SIGNATURES = {
+    "sa_forward": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I32P, _I32P, _I, _F, _I, _VP]),
+    "sa_forward_lse": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I32P, _I32P, _I, _F,
+                            _I, _VP]),
+    "sa_count_pairs": (_I, [_I, _I, _I32P, _I, _I32P, _I, _I64P, _I64P]),
+    "sa_last_error": (ctypes.c_char_p, []),
+    "sa_sync_status": (_I, [_VP]),
+    "sa_profile_begin": (_I, []),
+    "sa_profile_end": (_I, [ctypes.POINTER(_Profile)]),
+    "sa_version": (ctypes.c_char_p, []),
+}
+
+
+class SaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIBPATH
+
+
+def load(path: Optional[str] = None):
+    """Load the compiled library (build it first with ``build.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != SA_OK:
+        raise SaError(status, load().sa_last_error().decode(errors="replace"))
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32).reshape(-1))
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None or a.size == 0 else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def count_pairs(N: int, window: int, dilation: Sequence[int] | None, H: int,
+                globals_: Sequence[int] = ()):
+    """(per_head int64[H], total) -- exact in-mask pair counts (host only)."""
+    dil = None if dilation is None else _i32(dilation)
+    g = _i32(globals_)
+    per = np.zeros(H, dtype=np.int64)
+    tot = ctypes.c_int64(0)
+    _check(load().sa_count_pairs(int(N), int(window), _ptr(dil), int(H), _ptr(g), int(g.size),
+                                 _ptr(per), ctypes.byref(tot)))
+    return per, int(tot.value)
+
+
+def forward(q, k, v, window: int, dilation: Sequence[int] | None = None,
+            globals_: Sequence[int] = (), scale: Optional[float] = None, out=None,
+            lse=None, stream=None):
+    """out = sparse attention of torch CUDA tensors q, k, v ([B, H, N, D]).
+
+    ``lse``: None, or a float32 CUDA tensor [B, H, N] to receive log-sum-exp.
+    Runs on ``stream`` (default: torch's current stream); returns ``out``.
+    """
+    import torch
+
+    if q.dtype == torch.bfloat16:
+        dt = SA_BF16
+    elif q.dtype == torch.float32:
+        dt = SA_FP32
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype} (bfloat16 or float32)")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or t.shape != q.shape:
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one shape and dtype")
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, D]")
+    B, H, N, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    dil = None if dilation is None else _i32(dilation)
+    if dil is not None and dil.size != H:
+        raise ValueError("dilation needs one entry per head")
+    g = _i32(globals_)
+    sc = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    h_stream = ctypes.c_void_p(stream.cuda_stream)
+    with torch.cuda.device(q.device):
+        if lse is None:
+            st = load().sa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   B, H, N, D, int(window), _ptr(dil), _ptr(g), int(g.size),
+                                   sc, dt, h_stream)
+        else:
+            st = load().sa_forward_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                       lse.data_ptr(), B, H, N, D, int(window), _ptr(dil),
+                                       _ptr(g), int(g.size), sc, dt, h_stream)
+    _check(st)
+    return out
+
+
+def sync_status(stream=None):
+    import torch
+    s = stream or torch.cuda.current_stream()
+    _check(load().sa_sync_status(ctypes.c_void_p(s.cuda_stream)))
+
+
+def profile_begin():
+    _check(load().sa_profile_begin())
+
+
+def profile_end() -> dict:
+    prof = _Profile()
+    _check(load().sa_profile_end(ctypes.byref(prof)))
+    return {name: {"launches": int(prof.launches[i]), "ms": float(prof.ms[i])}
+            for i, name in enumerate(STAGES)}
+
+
+def version() -> str:
+    return load().sa_version().decode()
