@@ -135,6 +135,49 @@ typedef struct {
 sa_status sa_profile_begin(void);
 sa_status sa_profile_end(sa_profile *out);
 
+/*
+ * sa_forward_noalloc -- sa_forward_lse without any device memory allocation.
+ *
+ * No passage of the source pages corresponds to this call: it exists for
+ * callers that must not allocate device memory while they run attention --
+ * a host application that owns the whole device memory budget (for example
+ * through its own pool), an allocator-free plug-in or runtime, or code that
+ * runs where allocation is not allowed.  sa_forward takes its scratch (the
+ * band-tile work list, the gathered global rows, the split-K partial softmax
+ * statistics) from a library-owned pool and caches schedules in cudaMalloc'ed
+ * buffers; this call takes all of it from one static device array of
+ * SA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ *  Arguments, layouts, ownership and validation are those of sa_forward_lse
+ *  (lse may be NULL).  The arithmetic runs on the CUDA cores in fp32 for both
+ *  input types (bf16 in and out for SA_BF16), so results agree with
+ *  sa_forward_lse within the library's stated tolerance, not bit for bit.
+ *
+ *  Size limit: a problem whose scratch does not fit the array even after the
+ *  global-row pass is split into fewer key chunks is rejected with
+ *  SA_ERR_UNSUPPORTED and a message giving the bytes it needs; nothing is
+ *  launched.  (One 131072-long sequence with 16 heads, D = 128 and 64
+ *  globals fits.)
+ *
+ *  Set-up: the first call on each device looks up the device address of the
+ *  static array (with that device current).  Make that first call before any
+ *  stream capture begins.
+ *
+ *  Sharing: every call uses the same array, which keeps what the last call
+ *  left there.  Each call writes every scratch byte it later reads, so nothing
+ *  needs clearing between calls, but calls whose work overlaps on the GPU
+ *  (different streams, or different host threads) race on the array: order
+ *  them on one stream or synchronise between them.
+ */
+#define SA_NOALLOC_SCRATCH_BYTES (8u << 20)
+sa_status sa_forward_noalloc(const void *q, const void *k, const void *v, void *out,
+                             float *lse, int B, int H, int N, int D, int window,
+                             const int32_t *dilation, const int32_t *global_idx,
+                             int n_global, float scale, sa_dtype dtype,
+                             sa_stream_t stream);
+
 /* Library version string. */
 const char *sa_version(void);
 

@@ -327,6 +327,12 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
 }
 
 }  // namespace
+
+sa_status record_error(sa_status s, const char *message) {
+  t_last_error = message;
+  return s;
+}
+
 }  // namespace sa
 
 using namespace sa;

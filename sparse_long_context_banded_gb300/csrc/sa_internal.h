@@ -78,4 +78,7 @@ std::vector<int32_t> global_set(const int32_t *idx, int n);
 Schedule build_schedule(const Problem &p, const Tiling &t);
 int64_t pairs_of_head(int N, int half, int d, const std::vector<int32_t> &globals);
 
+// Sets the thread-local message that sa_last_error() returns; returns s.
+sa_status record_error(sa_status s, const char *message);
+
 }  // namespace sa

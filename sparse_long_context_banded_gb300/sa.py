@@ -42,7 +42,10 @@ SIGNATURES = {
     "sa_profile_begin": (_I, []),
     "sa_profile_end": (_I, [ctypes.POINTER(_Profile)]),
     "sa_version": (ctypes.c_char_p, []),
+    "sa_forward_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I32P, _I32P, _I,
+                                _F, _I, _VP]),
 }
+SA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class SaError(RuntimeError):
@@ -142,6 +145,33 @@ def forward(q, k, v, window: int, dilation: Sequence[int] | None = None,
             st = load().sa_forward_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                        lse.data_ptr(), B, H, N, D, int(window), _ptr(dil),
                                        _ptr(g), int(g.size), sc, dt, h_stream)
+    _check(st)
+    return out
+
+
+def forward_noalloc(q, k, v, window: int, dilation: Sequence[int] | None = None,
+                    globals_: Sequence[int] = (), scale: Optional[float] = None, out=None,
+                    lse=None, stream=None):
+    """Like ``forward``, through sa_forward_noalloc: the library allocates no
+    device memory and uses its static scratch array instead (see include/sa.h)."""
+    import torch
+
+    dt = SA_BF16 if q.dtype == torch.bfloat16 else SA_FP32 if q.dtype == torch.float32 else None
+    if dt is None:
+        raise TypeError(f"unsupported dtype {q.dtype} (bfloat16 or float32)")
+    B, H, N, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    dil = None if dilation is None else _i32(dilation)
+    g = _i32(globals_)
+    sc = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    with torch.cuda.device(q.device):
+        st = load().sa_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                       None if lse is None else lse.data_ptr(), B, H, N, D,
+                                       int(window), _ptr(dil), _ptr(g), int(g.size), sc, dt,
+                                       ctypes.c_void_p(stream.cuda_stream))
     _check(st)
     return out
 
