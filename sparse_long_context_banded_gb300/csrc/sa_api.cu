@@ -309,12 +309,13 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   };
   if (dp.n_g > 0) step(0, [&] { return launch_gather(dp, BH, dtype, stream); }, "gather launch");
   if (tc)
-    step(1, [&] { return launch_band_tc(dp, stream); }, "band (tensor-core) launch");
+    step(1, [&] { return launch_band_tc(dp, hs.slots.data(), (int)hs.slots.size(), hs.group_begin, BH, stream); },
+         "band (tensor-core) launch");
   else
     step(1, [&] { return launch_band_simt(dp, dtype, stream); }, "band launch");
   if (dp.n_g > 0) {
     if (tc)
-      step(2, [&] { return launch_global_tc(dp, stream); }, "global-row (tensor-core) launch");
+      step(2, [&] { return launch_global_tc(dp, BH, stream); }, "global-row (tensor-core) launch");
     else
       step(2, [&] { return launch_global_simt(dp, dtype, stream); }, "global-row launch");
     step(3, [&] { return launch_merge(dp, BH, dtype, stream); }, "merge launch");

@@ -55,18 +55,21 @@ struct Problem {
 
 // Tiling of one kernel family.
 struct Tiling {
-  int rows;        // query rows per tile
-  int q_tiles;     // query tiles per CTA (1 or 2)
-  int key_tile;    // keys per band tile
-  int g_tile;      // keys per global tile (and global query rows per tile)
-  int target_ctas; // CTAs wanted for the global-row pass
+  int rows;         // query rows per tile
+  int q_tiles;      // query tiles per CTA (1 or 2)
+  int key_tile;     // keys per band tile
+  int g_tile;       // the gathered global rows are padded to a multiple of this
+  int g_item_rows;  // global query rows per CTA of the global-row pass
+  int target_ctas;  // CTAs wanted for the global-row pass
+  int max_slots;    // residue classes one launch can address (groups items)
 };
 
 // Full launch schedule of one problem for one tiling.
 struct Schedule {
   std::vector<Slot> slots;
   std::vector<int32_t> head_slot0;  // first slot index of each head's dilation
-  std::vector<BandItem> band;
+  std::vector<BandItem> band;          // grouped by slot group, longest first
+  std::vector<int32_t> group_begin;    // band[group_begin[g] .. group_begin[g+1])
   std::vector<GlobalItem> global;
   int n_chunks = 0, chunk_len = 0, g_pad = 0;
   int64_t band_tile_pairs = 0;  // executed (query tile, key tile) pairs

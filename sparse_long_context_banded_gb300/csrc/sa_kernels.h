@@ -38,7 +38,7 @@ struct DevProblem {
 };
 
 // SIMT path (fp32 inputs): CUDA-core arithmetic, fp32 throughout.
-constexpr Tiling kSimtTiling{64, 1, 64, 64, 608};
+constexpr Tiling kSimtTiling{64, 1, 64, 64, 64, 608, 1 << 30};
 cudaError_t launch_gather(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s);
 cudaError_t launch_band_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s);
 cudaError_t launch_global_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s);

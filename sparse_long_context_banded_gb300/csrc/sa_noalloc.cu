@@ -156,7 +156,7 @@ extern "C" sa_status sa_forward_noalloc(const void *q, const void *k, const void
   Tiling t = kSimtTiling;
   Schedule s = build_schedule(p, t);
   Layout L = layout_of(p, s);
-  const int g_items = p.globals.empty() ? 1 : (int)((p.globals.size() + t.g_tile - 1) / t.g_tile);
+  const int g_items = p.globals.empty() ? 1 : (int)((p.globals.size() + t.g_item_rows - 1) / t.g_item_rows);
   while (L.total > kStaticScratchBytes && s.n_chunks > 1) {
     t.target_ctas = (s.n_chunks / 2) * B * H * g_items;
     s = build_schedule(p, t);

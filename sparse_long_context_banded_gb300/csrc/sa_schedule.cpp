@@ -151,29 +151,40 @@ Schedule build_schedule(const Problem &p, const Tiling &t) {
         }
       }
     }
-  // longest work first (stable, so equal-work items keep their sequence order
-  // and neighbouring CTAs keep sharing key/value tiles in L2)
+  // grouped by slot group (a launch addresses at most max_slots residue
+  // classes), then longest work first (stable, so equal-work items keep their
+  // sequence order and neighbouring CTAs keep sharing key/value tiles in L2)
+  auto group_of = [&t](const BandItem &it) { return it.slot / t.max_slots; };
   std::stable_sort(items.begin(), items.end(),
-                   [](const std::pair<int, BandItem> &a, const std::pair<int, BandItem> &b) {
+                   [&](const std::pair<int, BandItem> &a, const std::pair<int, BandItem> &b) {
+                     const int ga = group_of(a.second), gb = group_of(b.second);
+                     if (ga != gb) return ga < gb;
                      return a.first > b.first;
                    });
   s.band.reserve(items.size());
   for (auto &x : items) s.band.push_back(x.second);
+  const int n_groups = ((int)s.slots.size() + t.max_slots - 1) / t.max_slots;
+  s.group_begin.assign(n_groups + 1, 0);
+  for (size_t i = 0, g = 0; g <= (size_t)n_groups; ++g) {
+    while (i < s.band.size() && group_of(s.band[i]) < (int)g) ++i;
+    s.group_begin[g] = (int32_t)i;
+  }
+  s.group_begin[n_groups] = (int32_t)s.band.size();
 
   // global-row pass: split the N keys into chunks so that enough CTAs run
   if (n_g > 0) {
-    const int g_tiles = (n_g + t.g_tile - 1) / t.g_tile;
-    s.g_pad = g_tiles * t.g_tile;
+    s.g_pad = ((n_g + t.g_tile - 1) / t.g_tile) * t.g_tile;
+    const int g_items = (n_g + t.g_item_rows - 1) / t.g_item_rows;
     const int64_t bh = (int64_t)p.B * p.H;
     const int64_t max_chunks = (p.N + t.key_tile - 1) / t.key_tile;
-    int64_t want = (t.target_ctas + bh * g_tiles - 1) / (bh * g_tiles);
+    int64_t want = (t.target_ctas + bh * g_items - 1) / (bh * g_items);
     want = std::max<int64_t>(1, std::min(want, max_chunks));
     const int64_t per = (p.N + want - 1) / want;
     s.chunk_len = (int)(((per + t.key_tile - 1) / t.key_tile) * t.key_tile);
     s.n_chunks = (int)((p.N + s.chunk_len - 1) / s.chunk_len);
     for (int64_t x = 0; x < bh; ++x)
       for (int c = 0; c < s.n_chunks; ++c)
-        for (int gt = 0; gt < g_tiles; ++gt)
+        for (int gt = 0; gt < g_items; ++gt)
           s.global.push_back(GlobalItem{(int32_t)x, c, gt, 0});
   }
   return s;

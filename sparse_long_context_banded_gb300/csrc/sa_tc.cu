@@ -1,15 +1,881 @@
-// sa_tc.cu -- placeholder: routes bf16 to the CUDA-core kernels until the
-// tensor-core kernels land.
+// sa_tc.cu -- tensor-core kernels (sm_103a: TMA, mbarrier, tcgen05 + TMEM)
+// for bf16 inputs: the band-tile kernel and the global-row split-K kernel.
+//
+// What one CTA computes (Unlimiformer section 2.3 Eq. (1) under the additive
+// {0,-inf} mask of GMAT's "Global-Memory Augmented Transformers" section):
+// two 128-row query tiles Q_0, Q_1, each against its own list of key tiles --
+// the band tiles that intersect its rows' windows (Longformer glossary, "How the
+// Longformer attention works": sliding / dilated window) followed by the
+// gathered global keys (the same section's global attention; GMAT "Global
+// Memory") -- with an exact online softmax in fp32:
+//
+//   S = Q_u K_j^T (tcgen05, fp32 in TMEM) -> scale, mask (edge tiles only),
+//   running max / sum per row -> P = exp2(S - m) as bf16 written back into the
+//   same TMEM columns -> O_u += P V_j (tcgen05, A operand from TMEM).
+//
+// In global mode the two query tiles are the gathered global rows and the key
+// tiles one chunk of all N keys; the CTA writes unnormalised partial outputs
+// and their (max, sum) for the merge kernel.
+//
+// Warp roles (320 threads): warps 0-3 softmax of Q_0 (one thread per row),
+// warps 4-7 softmax of Q_1, warp 8 TMA producer, warp 9 MMA issuer (and TMEM
+// allocator).  TMEM: S_0 cols [0,128), S_1 [128,256), O_0 [256,256+D),
+// O_1 [384,384+D).  Shared memory: Q_0, Q_1, then a ring of key/value slots
+// (one K or V tile each), then barriers.  All tiles use the 128-byte swizzle
+// that TMA writes and the UMMA descriptors read.
+//
+// Every wait on an mbarrier is bounded: after kWaitLimitNs the waiting thread
+// sets the CTA's abort flag and the device error word, and every role winds
+// down (no trap, no endless spin).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
 #include "sa_tc.h"
 
 namespace sa {
+namespace tc {
 
-Tiling tc_tiling(int) { return kSimtTiling; }
-cudaError_t launch_band_tc(const DevProblem &p, cudaStream_t s) {
-  return launch_band_simt(p, SA_BF16, s);
+constexpr int kThreads = 320;
+constexpr int kRows = 128;         // query rows per tile (TMEM lanes)
+constexpr int kKeys = 128;         // keys per band tile
+constexpr int kGKeys = 64;         // keys per global tile
+constexpr int kMaxSlotsPerLaunch = 16;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kTmemCols = 512;
+
+struct Maps {
+  CUtensorMap q[kMaxSlotsPerLaunch], k[kMaxSlotsPerLaunch], v[kMaxSlotsPerLaunch],
+      o[kMaxSlotsPerLaunch];
+  CUtensorMap kg, vg;  // gathered global keys / values, 64-row boxes
+  CUtensorMap qg;      // gathered global queries, 128-row boxes
+  CUtensorMap kp, vp;  // plain (undilated) keys / values, 128-row boxes
+};
+
+struct Params {
+  Maps maps;
+  DevProblem p;
+  int slot_base;    // slot index held in maps.q[0]
+  int item_offset;  // first work item of this launch
+};
+
+template <int D>
+struct Cfg {
+  static constexpr int kQBytes = kRows * D * 2;    // one query tile
+  static constexpr int kSlotBytes = kKeys * D * 2; // one key or value tile
+  static constexpr int kHalfCols = 64;             // bf16 columns per 128-byte row
+  static constexpr int kHalves = D / 64;
+  static constexpr int kAux = 1024 + 2048;         // barriers, flags, global list; alignment
+  static constexpr int kSmemMax = 232448;
+  static constexpr int kSlots0 = (kSmemMax - 2 * kQBytes - kAux) / kSlotBytes;
+  static constexpr int kSlots = kSlots0 > 12 ? 12 : kSlots0;
+  static constexpr int kSmemBytes = 2 * kQBytes + kSlots * kSlotBytes + kAux;
+  static_assert(kSlots >= 4, "the key/value ring needs at least four slots");
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-cudaError_t launch_global_tc(const DevProblem &p, cudaStream_t s) {
-  return launch_global_simt(p, SA_BF16, s);
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait.  Returns false (and leaves the abort flag set) if the CTA is
+// aborting or the limit ran out.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                      int *err, bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = global_timer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0) {
+      if (honour_abort && *abort_flag) return false;
+      if (honour_abort && err && (*(volatile int *)err & kErrWaitTimeout)) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (global_timer() - start > kWaitLimitNs) {
+        *abort_flag = 1;
+        if (err) atomicOr(err, kErrWaitTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_commit_and_drain() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// AND of `v` over the `threads` threads that reach named barrier `id`.
+__device__ __forceinline__ bool named_bar_and(int id, int threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "setp.ne.u32 p, %1, 0;\n"
+      "bar.red.and.pred q, %2, %3, p;\n"
+      "selp.u32 %0, 1, 0, q;\n"
+      "}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane; the wait is fused so the
+// registers are valid when the statement completes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// UMMA shared-memory descriptor, 128-byte swizzle (SM100 layout, version 1).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor: bf16 x bf16 -> fp32, M x N, A K-major, B K- or MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// work description shared by all roles of one CTA
+
+struct Work {
+  int bh;
+  int slot;      // residue-class slot (band mode)
+  int d, r, len; // residue class: positions r + d*t, t < len (band mode)
+  int q_tile;    // first query tile (band mode)
+  int flags;     // bit u: global tile of query tile u needs the in-band test
+  int lo;        // first band tile of the CTA's list
+  int nb;        // band tiles in the list
+  int ng;        // global tiles in the list
+  int n_lo[2], n_cnt[2];  // per query tile: first band tile, band tile count
+  int active[2];
+  int key0;      // global mode: first key of the chunk
+  int key_end;   // global mode: one past the chunk's last key
+  int chunk;
+};
+
+template <bool GLOBAL>
+__device__ __forceinline__ Work make_work(const Params &P) {
+  Work w{};
+  const DevProblem &p = P.p;
+  if (!GLOBAL) {
+    const BandItem it = p.band[P.item_offset + blockIdx.x];
+    const Slot sl = p.slots[it.slot];
+    w.bh = it.bh;
+    w.slot = it.slot;
+    w.d = sl.d;
+    w.r = sl.r;
+    w.len = sl.len;
+    w.q_tile = it.q_tile;
+    w.flags = it.flags;
+    w.lo = it.k_lo[0];
+    int hi = it.k_hi[0];
+    for (int u = 0; u < 2; ++u) {
+      w.active[u] = it.k_hi[u] >= it.k_lo[u];
+      w.n_lo[u] = it.k_lo[u];
+      w.n_cnt[u] = w.active[u] ? it.k_hi[u] - it.k_lo[u] + 1 : 0;
+      if (w.active[u]) hi = max(hi, it.k_hi[u]);
+    }
+    w.nb = hi - w.lo + 1;
+    w.ng = (p.n_g + kGKeys - 1) / kGKeys;
+  } else {
+    const GlobalItem it = p.gitems[blockIdx.x];
+    w.bh = it.bh;
+    w.chunk = it.chunk;
+    w.key0 = it.chunk * p.chunk_len;
+    w.key_end = min(p.N, w.key0 + p.chunk_len);
+    w.lo = 0;
+    w.nb = (w.key_end - w.key0 + kKeys - 1) / kKeys;
+    w.ng = 0;
+    for (int u = 0; u < 2; ++u) {
+      w.active[u] = (it.g_tile * 2 + u) * kRows < p.n_g;
+      w.n_lo[u] = 0;
+      w.n_cnt[u] = w.active[u] ? w.nb : 0;
+    }
+  }
+  return w;
+}
+
+// Position in the CTA's tile list of the i-th tile of query tile u.
+__device__ __forceinline__ int seq_pos(const Work &w, int u, int i) {
+  return i < w.n_cnt[u] ? (w.n_lo[u] - w.lo + i) : (w.nb + (i - w.n_cnt[u]));
+}
+__device__ __forceinline__ int seq_len(const Work &w, int u) {
+  return w.active[u] ? w.n_cnt[u] + w.ng : 0;
+}
+// How many query tiles read list position pos.
+__device__ __forceinline__ int readers_of(const Work &w, int pos) {
+  if (pos >= w.nb) return (int)w.active[0] + (int)w.active[1];
+  const int j = w.lo + pos;
+  int n = 0;
+  for (int u = 0; u < 2; ++u)
+    n += (w.active[u] && j >= w.n_lo[u] && j < w.n_lo[u] + w.n_cnt[u]) ? 1 : 0;
+  return n;
+}
+
+struct Bars {
+  uint32_t slot_full, slot_empty;  // arrays of kSlots
+  uint32_t q_full, s_full, p_full, o_final, mma_done;
+};
+
+// ---------------------------------------------------------------------------
+// softmax: one key tile of W columns for one row
+
+template <int W>
+struct TileScores {
+  float s[W];
+};
+
+template <int D, bool GLOBAL>
+__global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_constant__ Params P) {
+  using C = Cfg<D>;
+  constexpr int NS = C::kSlots;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  const uint32_t s_q0 = smem_u32(smem);
+  const uint32_t s_slots = s_q0 + 2 * C::kQBytes;
+  uint8_t *aux = smem + 2 * C::kQBytes + NS * C::kSlotBytes;
+  uint64_t *bar_mem = reinterpret_cast<uint64_t *>(aux);  // 2*NS + 8 barriers
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(aux + 8 * (2 * NS + 8));
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(aux + 8 * (2 * NS + 8) + 4);
+  int32_t *g_list = reinterpret_cast<int32_t *>(aux + 8 * (2 * NS + 8) + 16);
+
+  Bars B;
+  B.slot_full = smem_u32(bar_mem);
+  B.slot_empty = B.slot_full + 8 * NS;
+  B.q_full = B.slot_empty + 8 * NS;
+  B.s_full = B.q_full + 8;   // [2]
+  B.p_full = B.s_full + 16;  // [2]
+  B.o_final = B.p_full + 16; // [2]
+  B.mma_done = B.o_final + 16;
+
+  const DevProblem &p = P.p;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const Work w = make_work<GLOBAL>(P);
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(B.slot_full + 8 * i, 1);
+      mbar_init(B.slot_empty + 8 * i, 1);
+    }
+    mbar_init(B.q_full, 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(B.s_full + 8 * u, 1);
+      mbar_init(B.p_full + 8 * u, 4);  // one arrival per softmax warp
+      mbar_init(B.o_final + 8 * u, 1);
+    }
+    mbar_init(B.mma_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (!GLOBAL)
+    for (int i = tid; i < p.n_g; i += kThreads) g_list[i] = p.globals[i];
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const CUtensorMap *map_q, *map_k, *map_v;
+  if (!GLOBAL) {
+    const int ls = w.slot - P.slot_base;
+    map_q = &P.maps.q[ls];
+    map_k = &P.maps.k[ls];
+    map_v = &P.maps.v[ls];
+  } else {
+    map_q = &P.maps.qg;
+    map_k = &P.maps.kp;
+    map_v = &P.maps.vp;
+  }
+
+  if (warp == 8) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      const int n_active = (int)w.active[0] + (int)w.active[1];
+      mbar_expect_tx(B.q_full, n_active * C::kQBytes);
+      for (int u = 0; u < 2; ++u) {
+        if (!w.active[u]) continue;
+        const int y = GLOBAL ? u * kRows : (w.q_tile + u) * kRows;
+        for (int h = 0; h < C::kHalves; ++h)
+          tma_load_3d(s_q0 + u * C::kQBytes + h * (kRows * 128), map_q, B.q_full, 64 * h, y, w.bh);
+      }
+      const int n_tiles = w.nb + w.ng;
+      int n = 0;
+      bool ok = true;
+      for (int pos = 0; pos < n_tiles && ok; ++pos) {
+        const bool gt = pos >= w.nb;
+        const int rows = gt ? kGKeys : kKeys;
+        const int y = gt ? (pos - w.nb) * kGKeys : (GLOBAL ? w.key0 + pos * kKeys : (w.lo + pos) * kKeys);
+        const CUtensorMap *mk = gt ? &P.maps.kg : map_k;
+        const CUtensorMap *mv = gt ? &P.maps.vg : map_v;
+        for (int which = 0; which < 2 && ok; ++which, ++n) {
+          const int s = n % NS, use = n / NS;
+          if (!wait_bar(B.slot_empty + 8 * s, (use & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = s_slots + s * C::kSlotBytes;
+          mbar_expect_tx(B.slot_full + 8 * s, rows * D * 2);
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(dst + h * (rows * 128), which ? mv : mk, B.slot_full + 8 * s, 64 * h, y,
+                        w.bh);
+        }
+      }
+      if (!ok) {
+        // drain the loads still in flight before the CTA's memory is released
+        for (int k = max(0, n - NS); k < n; ++k)
+          wait_bar(B.slot_full + 8 * (k % NS), (k / NS) & 1, abort_flag, nullptr, false);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = wait_bar(B.q_full, 0, abort_flag, p.err);
+      tc_fence_after();
+      int armed[NS], readers[NS];
+      for (int i = 0; i < NS; ++i) armed[i] = -1, readers[i] = 0;
+      int len_u[2] = {seq_len(w, 0), seq_len(w, 1)};
+      int pv_count[2] = {0, 0};
+      constexpr uint32_t kIdescS = idesc_bf16(kRows, kKeys, false);
+      constexpr uint32_t kIdescSg = idesc_bf16(kRows, kGKeys, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(kRows, D, true);
+
+      auto acquire = [&](int load) -> bool {
+        const int s = load % NS;
+        if (armed[s] != load) {
+          if (!wait_bar(B.slot_full + 8 * s, (load / NS) & 1, abort_flag, p.err)) return false;
+          tc_fence_after();
+          armed[s] = load;
+          readers[s] = readers_of(w, load >> 1);
+        }
+        return true;
+      };
+      auto release = [&](int load) {
+        const int s = load % NS;
+        if (--readers[s] == 0) mma_commit(B.slot_empty + 8 * s);
+      };
+      auto issue_s = [&](int u, int pos) -> bool {
+        const int load = 2 * pos;
+        if (!acquire(load)) return false;
+        const bool gt = pos >= w.nb;
+        const int rows = gt ? kGKeys : kKeys;
+        const uint32_t kbase = s_slots + (load % NS) * C::kSlotBytes;
+        const uint32_t qbase = s_q0 + u * C::kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_q = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
+          const uint32_t off_k = (kk >> 2) * (rows * 128) + (kk & 3) * 32;
+          mma_ss(tmem + u * 128, sw128_desc(qbase + off_q, 16, 1024),
+                 sw128_desc(kbase + off_k, 16, 1024), gt ? kIdescSg : kIdescS, kk > 0);
+        }
+        mma_commit(B.s_full + 8 * u);
+        release(load);
+        return true;
+      };
+      auto issue_pv = [&](int u, int pos, bool last) -> bool {
+        if (!wait_bar(B.p_full + 8 * u, pv_count[u] & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const int load = 2 * pos + 1;
+        if (!acquire(load)) return false;
+        const bool gt = pos >= w.nb;
+        const int rows = gt ? kGKeys : kKeys;
+        const uint32_t vbase = s_slots + (load % NS) * C::kSlotBytes;
+        for (int kk = 0; kk < rows / 16; ++kk) {
+          mma_ts(tmem + 256 + u * 128, tmem + u * 128 + kk * 8,
+                 sw128_desc(vbase + kk * 16 * 128, rows * 128, 1024), kIdescPV,
+                 (pv_count[u] > 0 || kk > 0) ? 1u : 0u);
+        }
+        ++pv_count[u];
+        release(load);
+        if (last) mma_commit(B.o_final + 8 * u);
+        return true;
+      };
+
+      int idx[2] = {0, 0};
+      for (int u = 0; u < 2 && ok; ++u)
+        if (len_u[u] > 0) ok = issue_s(u, seq_pos(w, u, 0));
+      while (ok && (idx[0] < len_u[0] || idx[1] < len_u[1])) {
+        for (int u = 0; u < 2 && ok; ++u) {
+          if (idx[u] >= len_u[u]) continue;
+          const int pos = seq_pos(w, u, idx[u]);
+          ++idx[u];
+          ok = issue_pv(u, pos, idx[u] == len_u[u]);
+          if (ok && idx[u] < len_u[u]) ok = issue_s(u, seq_pos(w, u, idx[u]));
+        }
+      }
+      // everything issued has completed before TMEM is released
+      mma_commit(B.mma_done);
+      wait_bar(B.mma_done, 0, abort_flag, nullptr, false);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int u = warp >> 2;
+    const int row = tid & 127;
+    const int wq = (tid & 127) >> 5;
+    const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_addr + u * 128;
+    const uint32_t t_o = tmem + lane_addr + 256 + u * 128;
+    const int n = seq_len(w, u);
+    const float sl = p.scale_log2;
+    const int t_q = GLOBAL ? 0 : (w.q_tile + u) * kRows + row;  // class coordinate
+    const int64_t pos_q = GLOBAL ? 0 : (int64_t)w.r + (int64_t)w.d * t_q;
+    const int half = p.half;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+
+    for (int i = 0; i < n && ok; ++i) {
+      const int pos = seq_pos(w, u, i);
+      const bool gt = pos >= w.nb;
+      ok = __all_sync(0xffffffffu, wait_bar(B.s_full + 8 * u, i & 1, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      float s[kKeys];
+      const int W = gt ? kGKeys : kKeys;
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < kKeys / 32; ++c) {
+          if (c * 32 < W) {
+            tmem_ld32(t_s + c * 32, r);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) s[c * 32 + x] = -INFINITY;
+          }
+        }
+      }
+      // scale into base-2 units, then mask
+      if (!gt) {
+        const int kb = GLOBAL ? (w.key0 + pos * kKeys) : (w.lo + pos) * kKeys;
+        bool full;
+        int c_lo = 0, c_hi = kKeys - 1;
+        if (GLOBAL) {
+          full = kb + kKeys <= w.key_end;
+          c_hi = w.key_end - 1 - kb;
+        } else {
+          const int q0 = (w.q_tile + u) * kRows;
+          full = (kb + kKeys - 1 - q0 <= half) && (q0 + kRows - 1 - kb <= half) &&
+                 (kb + kKeys <= w.len);
+          c_lo = t_q - half - kb;
+          c_hi = min(t_q + half, w.len - 1) - kb;
+        }
+        if (full) {
+#pragma unroll
+          for (int x = 0; x < kKeys; ++x) s[x] *= sl;
+        } else {
+#pragma unroll
+          for (int x = 0; x < kKeys; ++x) s[x] = (x >= c_lo && x <= c_hi) ? s[x] * sl : -INFINITY;
+        }
+      } else {
+        const int g0 = (pos - w.nb) * kGKeys;
+        const int c_hi = p.n_g - 1 - g0;
+        if (!((w.flags >> u) & 1)) {
+#pragma unroll
+          for (int x = 0; x < kGKeys; ++x) s[x] = (x <= c_hi) ? s[x] * sl : -INFINITY;
+        } else {
+          const int64_t reach = (int64_t)half * w.d;
+#pragma unroll
+          for (int x = 0; x < kGKeys; ++x) {
+            bool valid = x <= c_hi;
+            if (valid) {
+              const int64_t diff = pos_q - g_list[g0 + x];
+              const bool in_band = diff <= reach && -diff <= reach && (diff % w.d) == 0;
+              valid = !in_band;
+            }
+            s[x] = valid ? s[x] * sl : -INFINITY;
+          }
+        }
+      }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int x = 0; x < kKeys; ++x) mt = fmaxf(mt, s[x]);
+      // raise the reference maximum only when it grows by more than 2^8, so the
+      // accumulated output is rescaled rarely (exact: the same reference is
+      // used for the output and for the running sum)
+      const bool need = mt > m_run + 8.f;
+      const float m_new = need ? mt : m_run;
+      const float alpha = need ? ex2(m_run - m_new) : 1.f;
+      if (__any_sync(0xffffffffu, need && l_run > 0.f)) {
+        // O_u holds the previous tiles (their PV has completed: it was issued
+        // before this tile's S, whose completion we waited for)
+        const float a = (need && l_run > 0.f) ? alpha : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_o + c * 32, r);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * a);
+          tmem_st32(t_o + c * 32, r);
+        }
+      }
+      if (need) {
+        l_run *= alpha;
+        m_run = m_new;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float sum = 0.f;
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < kKeys / 64; ++c) {
+          if (c * 64 < W) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const float a0 = ex2(s[c * 64 + 2 * x] - m_use);
+              const float a1 = ex2(s[c * 64 + 2 * x + 1] - m_use);
+              sum += a0 + a1;
+              r[x] = pack_bf16(a0, a1);
+            }
+            tmem_st32(t_s + c * 32, r);
+          }
+        }
+      }
+      l_run += sum;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.p_full + 8 * u);
+    }
+
+    if (n > 0) {
+      // every thread of the warpgroup takes part in the same barriers, so the
+      // decision to write the tile is made jointly
+      bool fin = ok && wait_bar(B.o_final + 8 * u, 0, abort_flag, p.err);
+      fin = named_bar_and(1 + u, 128, fin);
+      if (fin) tc_fence_after();
+      if (!GLOBAL) {
+        // normalise, stage the bf16 tile in this query tile's (now idle) smem
+        // in the TMA 128-byte-swizzle layout, and store it with TMA
+        uint8_t *stage = smem + u * C::kQBytes;
+        if (fin) {
+          const float inv = 1.f / l_run;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(t_o + c * 32, r);
+            const int h = (c * 32) / 64;
+            const int chunk0 = ((c * 32) % 64) / 8;  // first 16-byte chunk in the row
+            uint8_t *rowp = stage + h * (kRows * 128) + row * 128;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(r[q4 * 8 + 0]) * inv, __uint_as_float(r[q4 * 8 + 1]) * inv);
+              v.y = pack_bf16(__uint_as_float(r[q4 * 8 + 2]) * inv, __uint_as_float(r[q4 * 8 + 3]) * inv);
+              v.z = pack_bf16(__uint_as_float(r[q4 * 8 + 4]) * inv, __uint_as_float(r[q4 * 8 + 5]) * inv);
+              v.w = pack_bf16(__uint_as_float(r[q4 * 8 + 6]) * inv, __uint_as_float(r[q4 * 8 + 7]) * inv);
+              const int phys = (chunk0 + q4) ^ (row & 7);
+              *reinterpret_cast<uint4 *>(rowp + phys * 16) = v;
+            }
+          }
+          if (p.lse && t_q < w.len)
+            p.lse[(int64_t)w.bh * p.N + pos_q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+          fence_proxy_async_smem();
+        }
+        named_bar_sync(1 + u, 128);
+        if (fin && row == 0) {
+          const int ls = w.slot - P.slot_base;
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_store_3d(&P.maps.o[ls], smem_u32(stage) + h * (kRows * 128), 64 * h,
+                         (w.q_tile + u) * kRows, w.bh);
+          tma_store_commit_and_drain();
+        }
+      } else if (fin) {
+        const int g = u * kRows + row;
+        const int64_t slot = ((int64_t)w.bh * p.n_chunks + w.chunk) * p.g_pad + g;
+        float4 *dst = reinterpret_cast<float4 *>(p.part_o + slot * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_o + c * 32, r);  // collective: every lane loads
+          if (g < p.n_g) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              dst[c * 8 + x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                                           __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+          }
+        }
+        if (g < p.n_g) {
+          p.part_ml[slot * 2 + 0] = m_run;
+          p.part_ml[slot * 2 + 1] = l_run;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// 3-D bf16 map {D, rows, bh}, 128-byte swizzle, boxes of {64, box_rows, 1}.
+cudaError_t make_map(CUtensorMap *m, const void *base, int D, uint64_t rows, uint64_t bh,
+                     uint64_t row_stride_bytes, uint64_t bh_stride_bytes, uint32_t box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, rows, bh};
+  cuuint64_t strides[2] = {row_stride_bytes, bh_stride_bytes};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, bool GLOBAL>
+cudaError_t launch(Params &P, int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  constexpr int smem = Cfg<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(tc_attention_kernel<D, GLOBAL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  tc_attention_kernel<D, GLOBAL><<<grid, kThreads, smem, s>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+Tiling tc_tiling(int) { return Tiling{tc::kRows, 2, tc::kKeys, 128, 256, 2 * 152, tc::kMaxSlotsPerLaunch}; }
+
+namespace {
+
+cudaError_t fill_common(tc::Params &P, const DevProblem &p, int BH) {
+  cudaError_t e = tc::get_encoder();
+  if (e != cudaSuccess) return e;
+  std::memset(&P.maps, 0, sizeof P.maps);
+  P.p = p;
+  P.p.half = std::min(p.half, p.N);  // a wider window changes nothing
+  const int D = p.D;
+  const uint64_t head = (uint64_t)p.N * D * 2;
+  if (p.n_g > 0) {
+    const uint64_t ghead = (uint64_t)p.g_pad * D * 2;
+    if ((e = tc::make_map(&P.maps.kg, p.kg, D, p.g_pad, BH, D * 2, ghead, tc::kGKeys)) ||
+        (e = tc::make_map(&P.maps.vg, p.vg, D, p.g_pad, BH, D * 2, ghead, tc::kGKeys)) ||
+        (e = tc::make_map(&P.maps.qg, p.qg, D, p.g_pad, BH, D * 2, ghead, tc::kRows)))
+      return e;
+  }
+  if ((e = tc::make_map(&P.maps.kp, p.k, D, p.N, BH, D * 2, head, tc::kKeys)) ||
+      (e = tc::make_map(&P.maps.vp, p.v, D, p.N, BH, D * 2, head, tc::kKeys)))
+    return e;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_band_tc(const DevProblem &p, const Slot *host_slots, int n_slots,
+                           const std::vector<int32_t> &group_begin, int BH, cudaStream_t s) {
+  static thread_local tc::Params P;  // ~9 KB of tensor maps: keep it off the stack
+  cudaError_t e = fill_common(P, p, BH);
+  if (e != cudaSuccess) return e;
+  const int D = p.D;
+  const uint64_t head = (uint64_t)p.N * D * 2;
+  const int n_groups = (int)group_begin.size() - 1;
+  for (int g = 0; g < n_groups; ++g) {
+    const int first = g * tc::kMaxSlotsPerLaunch;
+    const int count = std::min(tc::kMaxSlotsPerLaunch, n_slots - first);
+    for (int i = 0; i < count; ++i) {
+      const Slot &sl = host_slots[first + i];
+      const uint64_t off = (uint64_t)sl.r * D * 2;
+      const uint64_t stride = (uint64_t)sl.d * D * 2;
+      const char *q = static_cast<const char *>(p.q) + off;
+      const char *k = static_cast<const char *>(p.k) + off;
+      const char *v = static_cast<const char *>(p.v) + off;
+      char *o = static_cast<char *>(p.out) + off;
+      if ((e = tc::make_map(&P.maps.q[i], q, D, sl.len, BH, stride, head, tc::kRows)) ||
+          (e = tc::make_map(&P.maps.k[i], k, D, sl.len, BH, stride, head, tc::kKeys)) ||
+          (e = tc::make_map(&P.maps.v[i], v, D, sl.len, BH, stride, head, tc::kKeys)) ||
+          (e = tc::make_map(&P.maps.o[i], o, D, sl.len, BH, stride, head, tc::kRows)))
+        return e;
+    }
+    P.slot_base = first;
+    P.item_offset = group_begin[g];
+    const int grid = group_begin[g + 1] - group_begin[g];
+    e = D == 64 ? tc::launch<64, false>(P, grid, s) : tc::launch<128, false>(P, grid, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_global_tc(const DevProblem &p, int BH, cudaStream_t s) {
+  static thread_local tc::Params P;
+  cudaError_t e = fill_common(P, p, BH);
+  if (e != cudaSuccess) return e;
+  P.slot_base = 0;
+  P.item_offset = 0;
+  return p.D == 64 ? tc::launch<64, true>(P, p.n_gitems, s)
+                   : tc::launch<128, true>(P, p.n_gitems, s);
 }
 
 }  // namespace sa
