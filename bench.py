@@ -17,6 +17,7 @@ rows of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -47,6 +48,9 @@ def parse():
     ap.add_argument("--oracle-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run the workload with this many heads (profiling a smaller case)")
     return ap.parse_args()
 
 
@@ -237,6 +241,8 @@ def run_ours(args):
     sa.load()
 
     w = inputs.workload(args.workload)
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads, dilation=w.dilation[:1] * args.heads)
     # each rank runs its own independent batch of the workload (weak scaling)
     qkv = inputs.draw_qkv(w, seed=(1000 + w.number) if rank == 0 else (1000 + w.number + 7919 * rank))
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -317,7 +323,7 @@ def run_ours(args):
                "ms_per_step": ms_e2e / e2e_steps, "steps": e2e_steps}
 
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, secs, rows, threads = oracle_sample_timing(w, qkv, args.oracle_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} uniformly drawn query rows of {w.B * w.H * w.N}, "

@@ -39,17 +39,19 @@
 #include <mutex>
 
 #include "sa_tc.h"
+#include "sa_tmem_ops.h"
 
 namespace sa {
 namespace tc {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;     // ten warps: 168 registers per thread
 constexpr int kRows = 128;         // query rows per tile (TMEM lanes)
 constexpr int kKeys = 128;         // keys per band tile
 constexpr int kGKeys = 64;         // keys per global tile
 constexpr int kMaxSlotsPerLaunch = 16;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
+constexpr int kFarAway = -(1 << 30);  // class coordinate of a global outside the class
 
 struct Maps {
   CUtensorMap q[kMaxSlotsPerLaunch], k[kMaxSlotsPerLaunch], v[kMaxSlotsPerLaunch],
@@ -118,7 +120,7 @@ __device__ __forceinline__ uint64_t global_timer() {
 
 // Bounded wait.  Returns false (and leaves the abort flag set) if the CTA is
 // aborting or the limit ran out.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                       int *err, bool honour_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer();
@@ -228,34 +230,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-// 32 consecutive TMEM columns of this thread's lane; the wait is fused so the
-// registers are valid when the statement completes.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-      "%29, %30, %31, %32};\n" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -263,6 +237,11 @@ __device__ __forceinline__ void tmem_wait_st() {
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -372,6 +351,105 @@ struct TileScores {
   float s[W];
 };
 
+// One key tile of W columns for one query row (this thread's TMEM lane):
+// load S, mask, update the running maximum (rescaling O in TMEM when the
+// reference maximum moves), write P = 2^(scale*S - m) as bf16 over S, and add
+// its row sum.  Scores stay in base-2 units: scale is scale*log2(e).
+//   mask_mode 0: no mask.  1: keep columns [c_lo, c_hi].  2: global tile --
+//   keep columns <= c_hi whose global position is not already in the row's band.
+enum { kMaskNone = 0, kMaskInterval = 1, kMaskGlobal = 2 };
+
+template <int W, int D>
+__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float scale,
+                                             int mask_mode, int c_lo, int c_hi,
+                                             const int32_t *g_list, int g0, int t_q, int half,
+                                             bool dedup, float &m_run, float &l_run) {
+  float s[W];
+  {
+    uint32_t r[W];
+    if constexpr (W == 128)
+      tmem_ld128(t_s, r);
+    else
+      tmem_ld64(t_s, r);
+#pragma unroll
+    for (int x = 0; x < W; ++x) s[x] = __uint_as_float(r[x]);
+  }
+  float scl = scale;
+  if (scale < 0.f) {  // general path: scale first so that the maximum is taken on scaled scores
+#pragma unroll
+    for (int x = 0; x < W; ++x) s[x] *= scale;
+    scl = 1.f;
+  }
+  if (mask_mode == kMaskInterval) {
+#pragma unroll
+    for (int x = 0; x < W; ++x)
+      if (x < c_lo || x > c_hi) s[x] = -INFINITY;
+  } else if (mask_mode == kMaskGlobal) {
+#pragma unroll
+    for (int x = 0; x < W; ++x) {
+      bool valid = x <= c_hi;
+      if (valid && dedup) {
+        const int diff = t_q - g_list[g0 + x];  // class coordinates; kFarAway never in band
+        valid = diff > half || -diff > half;
+      }
+      if (!valid) s[x] = -INFINITY;
+    }
+  }
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+  for (int x = 8; x < W; x += 8)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[x + i]);
+  float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  mt *= scl;
+  // raise the reference maximum only when it grows by more than 2^8, so the
+  // accumulated output is rescaled rarely (exact: the same reference is used
+  // for the output and for the running sum); P of this tile is taken against
+  // the new reference, and O (older tiles) is brought to it below
+  const bool need = mt > m_run + 8.f;
+  const float m_new = need ? mt : m_run;
+  const float alpha = need ? ex2(m_run - m_new) : 1.f;
+  const bool rescale = need && l_run > 0.f;
+  const float neg = (m_new == -INFINITY) ? 0.f : -m_new;
+  float sum[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+  {
+    uint32_t pr[W / 2];
+#pragma unroll
+    for (int i = 0; i < W / 2; ++i) {
+      const float a0 = ex2(fmaf(s[2 * i], scl, neg));
+      const float a1 = ex2(fmaf(s[2 * i + 1], scl, neg));
+      sum[(2 * i) & 7] += a0;
+      sum[(2 * i + 1) & 7] += a1;
+      pr[i] = pack_bf16(a0, a1);
+    }
+    if constexpr (W == 128)
+      tmem_st64(t_s, pr);
+    else
+      tmem_st32(t_s, pr);
+  }
+  const float tile_sum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+  l_run = (need ? l_run * alpha : l_run) + tile_sum;
+  m_run = m_new;
+  if (__any_sync(0xffffffffu, rescale)) {
+    // O holds the previous tiles (their PV was issued before this tile's S,
+    // whose completion has been observed); bring it to the new reference
+    const float a = rescale ? alpha : 1.f;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(t_o + c * 32, r);
+#pragma unroll
+      for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * a);
+      tmem_st32(t_o + c * 32, r);
+    }
+  }
+}
+
 template <int D, bool GLOBAL>
 __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_constant__ Params P) {
   using C = Cfg<D>;
@@ -416,8 +494,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (!GLOBAL)
-    for (int i = tid; i < p.n_g; i += kThreads) g_list[i] = p.globals[i];
+  if (!GLOBAL) {
+    // global positions in this CTA's residue-class coordinates: g = r + d*t
+    // gives t; a global outside the class can never lie in a row's band
+    for (int i = tid; i < p.n_g; i += kThreads) {
+      const int g = p.globals[i] - w.r;
+      g_list[i] = (g >= 0 && g % w.d == 0) ? g / w.d : kFarAway;
+    }
+  }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
@@ -558,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
       mma_commit(B.mma_done);
       wait_bar(B.mma_done, 0, abort_flag, nullptr, false);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------- softmax
     const int u = warp >> 2;
     const int row = tid & 127;
@@ -580,23 +664,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
       ok = __all_sync(0xffffffffu, wait_bar(B.s_full + 8 * u, i & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      float s[kKeys];
-      const int W = gt ? kGKeys : kKeys;
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c) {
-          if (c * 32 < W) {
-            tmem_ld32(t_s + c * 32, r);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
-          } else {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) s[c * 32 + x] = -INFINITY;
-          }
-        }
-      }
-      // scale into base-2 units, then mask
       if (!gt) {
         const int kb = GLOBAL ? (w.key0 + pos * kKeys) : (w.lo + pos) * kKeys;
         bool full;
@@ -611,78 +678,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           c_lo = t_q - half - kb;
           c_hi = min(t_q + half, w.len - 1) - kb;
         }
-        if (full) {
-#pragma unroll
-          for (int x = 0; x < kKeys; ++x) s[x] *= sl;
-        } else {
-#pragma unroll
-          for (int x = 0; x < kKeys; ++x) s[x] = (x >= c_lo && x <= c_hi) ? s[x] * sl : -INFINITY;
-        }
+        softmax_tile<kKeys, D>(t_s, t_o, sl, full ? kMaskNone : kMaskInterval, c_lo, c_hi,
+                               nullptr, 0, 0, 0, false, m_run, l_run);
       } else {
         const int g0 = (pos - w.nb) * kGKeys;
-        const int c_hi = p.n_g - 1 - g0;
-        if (!((w.flags >> u) & 1)) {
-#pragma unroll
-          for (int x = 0; x < kGKeys; ++x) s[x] = (x <= c_hi) ? s[x] * sl : -INFINITY;
-        } else {
-          const int64_t reach = (int64_t)half * w.d;
-#pragma unroll
-          for (int x = 0; x < kGKeys; ++x) {
-            bool valid = x <= c_hi;
-            if (valid) {
-              const int64_t diff = pos_q - g_list[g0 + x];
-              const bool in_band = diff <= reach && -diff <= reach && (diff % w.d) == 0;
-              valid = !in_band;
-            }
-            s[x] = valid ? s[x] * sl : -INFINITY;
-          }
-        }
+        const bool dedup = (w.flags >> u) & 1;
+        softmax_tile<kGKeys, D>(t_s, t_o, sl, kMaskGlobal, 0, p.n_g - 1 - g0, g_list, g0, t_q,
+                                half, dedup, m_run, l_run);
       }
-      float mt = -INFINITY;
-#pragma unroll
-      for (int x = 0; x < kKeys; ++x) mt = fmaxf(mt, s[x]);
-      // raise the reference maximum only when it grows by more than 2^8, so the
-      // accumulated output is rescaled rarely (exact: the same reference is
-      // used for the output and for the running sum)
-      const bool need = mt > m_run + 8.f;
-      const float m_new = need ? mt : m_run;
-      const float alpha = need ? ex2(m_run - m_new) : 1.f;
-      if (__any_sync(0xffffffffu, need && l_run > 0.f)) {
-        // O_u holds the previous tiles (their PV has completed: it was issued
-        // before this tile's S, whose completion we waited for)
-        const float a = (need && l_run > 0.f) ? alpha : 1.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c * 32, r);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * a);
-          tmem_st32(t_o + c * 32, r);
-        }
-      }
-      if (need) {
-        l_run *= alpha;
-        m_run = m_new;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float sum = 0.f;
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < kKeys / 64; ++c) {
-          if (c * 64 < W) {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              const float a0 = ex2(s[c * 64 + 2 * x] - m_use);
-              const float a1 = ex2(s[c * 64 + 2 * x + 1] - m_use);
-              sum += a0 + a1;
-              r[x] = pack_bf16(a0, a1);
-            }
-            tmem_st32(t_s + c * 32, r);
-          }
-        }
-      }
-      l_run += sum;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -700,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
         // in the TMA 128-byte-swizzle layout, and store it with TMA
         uint8_t *stage = smem + u * C::kQBytes;
         if (fin) {
-          const float inv = 1.f / l_run;
+          const float inv = rcp_approx(l_run);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
