@@ -17,9 +17,9 @@
 // tiles one chunk of all N keys; the CTA writes unnormalised partial outputs
 // and their (max, sum) for the merge kernel.
 //
-// Warp roles (320 threads): warps 0-3 softmax of Q_0 (one thread per row),
-// warps 4-7 softmax of Q_1, warp 8 TMA producer, warp 9 MMA issuer (and TMEM
-// allocator).  TMEM: S_0 cols [0,128), S_1 [128,256), O_0 [256,256+D),
+// Warp roles (352 threads): warps 0-3 softmax of Q_0 (one thread per row),
+// warps 4-7 softmax of Q_1, warp 8 TMA producer, warp 9 MMA issuer of Q_0 (and
+// TMEM allocator), warp 10 MMA issuer of Q_1.  TMEM: S_0 cols [0,128), S_1 [128,256), O_0 [256,256+D),
 // O_1 [384,384+D).  Shared memory: Q_0, Q_1, then a ring of key/value slots
 // (one K or V tile each), then barriers.  All tiles use the 128-byte swizzle
 // that TMA writes and the UMMA descriptors read.
@@ -44,7 +44,7 @@
 namespace sa {
 namespace tc {
 
-constexpr int kThreads = 320;     // ten warps: 168 registers per thread
+constexpr int kThreads = 352;     // eleven warps: 168 registers per thread
 constexpr int kRows = 128;         // query rows per tile (TMEM lanes)
 constexpr int kKeys = 128;         // keys per band tile
 constexpr int kGKeys = 64;         // keys per global tile
@@ -74,7 +74,7 @@ struct Cfg {
   static constexpr int kSlotBytes = kKeys * D * 2; // one key or value tile
   static constexpr int kHalfCols = 64;             // bf16 columns per 128-byte row
   static constexpr int kHalves = D / 64;
-  static constexpr int kAux = 1024 + 2048;         // barriers, flags, global list; alignment
+  static constexpr int kAux = 3072;  // barriers, flags, global positions (class coordinates)
   static constexpr int kSmemMax = 232448;
   static constexpr int kSlots0 = (kSmemMax - 2 * kQBytes - kAux) / kSlotBytes;
   static constexpr int kSlots = kSlots0 > 12 ? 12 : kSlots0;
@@ -239,6 +239,11 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -321,6 +326,11 @@ __device__ __forceinline__ Work make_work(const Params &P) {
   return w;
 }
 
+// Position in the CTA's tile list of the i-th tile of a query tile whose band
+// tiles start at n_lo (n_cnt of them).
+__device__ __forceinline__ int seq_pos_s(const Work &w, int n_lo, int n_cnt, int i) {
+  return i < n_cnt ? (n_lo - w.lo + i) : (w.nb + (i - n_cnt));
+}
 // Position in the CTA's tile list of the i-th tile of query tile u.
 __device__ __forceinline__ int seq_pos(const Work &w, int u, int i) {
   return i < w.n_cnt[u] ? (w.n_lo[u] - w.lo + i) : (w.nb + (i - w.n_cnt[u]));
@@ -328,19 +338,9 @@ __device__ __forceinline__ int seq_pos(const Work &w, int u, int i) {
 __device__ __forceinline__ int seq_len(const Work &w, int u) {
   return w.active[u] ? w.n_cnt[u] + w.ng : 0;
 }
-// How many query tiles read list position pos.
-__device__ __forceinline__ int readers_of(const Work &w, int pos) {
-  if (pos >= w.nb) return (int)w.active[0] + (int)w.active[1];
-  const int j = w.lo + pos;
-  int n = 0;
-  for (int u = 0; u < 2; ++u)
-    n += (w.active[u] && j >= w.n_lo[u] && j < w.n_lo[u] + w.n_cnt[u]) ? 1 : 0;
-  return n;
-}
-
 struct Bars {
   uint32_t slot_full, slot_empty;  // arrays of kSlots
-  uint32_t q_full, s_full, p_full, o_final, mma_done;
+  uint32_t q_full, s_full, p_full, o_final, mma_done, s_issued;
 };
 
 // ---------------------------------------------------------------------------
@@ -359,26 +359,31 @@ struct TileScores {
 //   keep columns <= c_hi whose global position is not already in the row's band.
 enum { kMaskNone = 0, kMaskInterval = 1, kMaskGlobal = 2 };
 
-template <int W, int D>
-__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float scale,
-                                             int mask_mode, int c_lo, int c_hi,
-                                             const int32_t *g_list, int g0, int t_q, int half,
-                                             bool dedup, float &m_run, float &l_run) {
-  float s[W];
+// W scores of this thread's row from TMEM, scaled (negative scales only: a
+// positive scale is folded into the exponent) and masked to -inf.
+//   mask_mode 0: no mask.  1: keep columns [c_lo, c_hi].  2: global keys --
+//   keep columns <= c_hi whose global position is not already in the row's band
+//   (globals[g0 + x] is the global's class coordinate t_g, or kFarAway; the row
+//   is class position t_q, and the global is in its band when |t_q - t_g| <= half).
+template <int W>
+__device__ __forceinline__ void load_scores(uint32_t t_s, float scale, int mask_mode, int c_lo,
+                                            int c_hi, const int32_t *globals, int g0, int t_q,
+                                            int half, int cls_r, int cls_d, bool dedup,
+                                            float (&s)[W]) {
   {
     uint32_t r[W];
     if constexpr (W == 128)
       tmem_ld128(t_s, r);
-    else
+    else if constexpr (W == 64)
       tmem_ld64(t_s, r);
+    else
+      tmem_ld32(t_s, r);
 #pragma unroll
     for (int x = 0; x < W; ++x) s[x] = __uint_as_float(r[x]);
   }
-  float scl = scale;
   if (scale < 0.f) {  // general path: scale first so that the maximum is taken on scaled scores
 #pragma unroll
     for (int x = 0; x < W; ++x) s[x] *= scale;
-    scl = 1.f;
   }
   if (mask_mode == kMaskInterval) {
 #pragma unroll
@@ -389,51 +394,68 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
     for (int x = 0; x < W; ++x) {
       bool valid = x <= c_hi;
       if (valid && dedup) {
-        const int diff = t_q - g_list[g0 + x];  // class coordinates; kFarAway never in band
+        const int diff = t_q - globals[g0 + x];  // class coordinates; kFarAway is never in band
         valid = diff > half || -diff > half;
       }
       if (!valid) s[x] = -INFINITY;
     }
   }
+}
+
+// One key tile of W columns for one query row (this thread's TMEM lane):
+// P = 2^(scale*S - m) as bf16 written over S, running maximum m and row sum l
+// updated, O in TMEM rescaled when the reference maximum moves.  Scores are in
+// base-2 units (scale = scale*log2(e)).  The reference maximum is raised only
+// when the tile maximum exceeds it by more than 2^8, so O is rescaled rarely;
+// the same reference is used for P and for the running sum, so the result is
+// exact either way.
+template <int W, int D>
+__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float scale,
+                                             int mask_mode, int c_lo, int c_hi,
+                                             const int32_t *globals, int g0, int t_q, int half,
+                                             int cls_r, int cls_d, bool dedup, float &m_run,
+                                             float &l_run) {
+  const float scl = scale < 0.f ? 1.f : scale;
+  float s[W];
+  load_scores<W>(t_s, scale, mask_mode, c_lo, c_hi, globals, g0, t_q, half, cls_r, cls_d, dedup, s);
+  // row maximum: eight chains of three-input max
   float mx[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) mx[i] = s[i];
+  for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-  for (int x = 8; x < W; x += 8)
+  for (int x = 16; x < W; x += 16)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[x + i]);
-  float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-  mt *= scl;
-  // raise the reference maximum only when it grows by more than 2^8, so the
-  // accumulated output is rescaled rarely (exact: the same reference is used
-  // for the output and for the running sum); P of this tile is taken against
-  // the new reference, and O (older tiles) is brought to it below
+    for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[x + 2 * i], s[x + 2 * i + 1]);
+  const float mt =
+      max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * scl;
   const bool need = mt > m_run + 8.f;
   const float m_new = need ? mt : m_run;
   const float alpha = need ? ex2(m_run - m_new) : 1.f;
-  const bool rescale = need && l_run > 0.f;
+  const bool rescale = need && m_run != -INFINITY;  // O holds earlier tiles of this row
+  // P: the argument two columns at a time (packed fp32x2 FMA), the exponential
+  // on the SFU, row sums in four packed accumulators
   const float neg = (m_new == -INFINITY) ? 0.f : -m_new;
-  float sum[8];
+  const float2 scl2 = make_float2(scl, scl), neg2 = make_float2(neg, neg);
+  float2 sum2[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+  for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
   {
     uint32_t pr[W / 2];
 #pragma unroll
     for (int i = 0; i < W / 2; ++i) {
-      const float a0 = ex2(fmaf(s[2 * i], scl, neg));
-      const float a1 = ex2(fmaf(s[2 * i + 1], scl, neg));
-      sum[(2 * i) & 7] += a0;
-      sum[(2 * i + 1) & 7] += a1;
-      pr[i] = pack_bf16(a0, a1);
+      const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
+      const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
+      sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
+      pr[i] = pack_bf16(e.x, e.y);
     }
     if constexpr (W == 128)
       tmem_st64(t_s, pr);
     else
       tmem_st32(t_s, pr);
   }
-  const float tile_sum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-  l_run = (need ? l_run * alpha : l_run) + tile_sum;
+  const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+  const float2 s4 = __fadd2_rn(s01, s23);
+  l_run = (need ? l_run * alpha : l_run) + (s4.x + s4.y);
   m_run = m_new;
   if (__any_sync(0xffffffffu, rescale)) {
     // O holds the previous tiles (their PV was issued before this tile's S,
@@ -454,17 +476,16 @@ template <int D, bool GLOBAL>
 __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_constant__ Params P) {
   using C = Cfg<D>;
   constexpr int NS = C::kSlots;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw;
   const uint32_t s_q0 = smem_u32(smem);
   const uint32_t s_slots = s_q0 + 2 * C::kQBytes;
   uint8_t *aux = smem + 2 * C::kQBytes + NS * C::kSlotBytes;
-  uint64_t *bar_mem = reinterpret_cast<uint64_t *>(aux);  // 2*NS + 8 barriers
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(aux + 8 * (2 * NS + 8));
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(aux + 8 * (2 * NS + 8) + 4);
-  int32_t *g_list = reinterpret_cast<int32_t *>(aux + 8 * (2 * NS + 8) + 16);
-
+  uint64_t *bar_mem = reinterpret_cast<uint64_t *>(aux);  // 2*NS + 12 barriers
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(aux + 8 * (2 * NS + 12));
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(aux + 8 * (2 * NS + 12) + 4);
+  int32_t *g_list = reinterpret_cast<int32_t *>(aux + 1024);  // SA_MAX_GLOBALS entries
+  static_assert(8 * (2 * NS + 12) + 16 <= 1024 && 1024 + 4 * SA_MAX_GLOBALS <= C::kAux, "aux layout");
   Bars B;
   B.slot_full = smem_u32(bar_mem);
   B.slot_empty = B.slot_full + 8 * NS;
@@ -472,25 +493,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
   B.s_full = B.q_full + 8;   // [2]
   B.p_full = B.s_full + 16;  // [2]
   B.o_final = B.p_full + 16; // [2]
-  B.mma_done = B.o_final + 16;
+  B.mma_done = B.o_final + 16;  // [2]
+  B.s_issued = B.mma_done + 16; // [2]
 
   const DevProblem &p = P.p;
   const int tid = threadIdx.x;
+  if (s_q0 & 1023u) {  // 128-byte-swizzled tiles need 1024-byte alignment
+    if (tid == 0 && p.err) atomicOr(p.err, kErrBadWork);
+    return;
+  }
   const int warp = tid >> 5, lane = tid & 31;
   const Work w = make_work<GLOBAL>(P);
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(B.slot_full + 8 * i, 1);
-      mbar_init(B.slot_empty + 8 * i, 1);
+      mbar_init(B.slot_empty + 8 * i, w.active[1] ? 2 : 1);  // one arrival per issuing warp
     }
     mbar_init(B.q_full, 1);
     for (int u = 0; u < 2; ++u) {
       mbar_init(B.s_full + 8 * u, 1);
-      mbar_init(B.p_full + 8 * u, 4);  // one arrival per softmax warp
+      mbar_init(B.p_full + 8 * u, 4);  // one arrival per softmax warp of the tile's warpgroup
       mbar_init(B.o_final + 8 * u, 1);
     }
     mbar_init(B.mma_done, 1);
+    mbar_init(B.mma_done + 8, 1);
+    mbar_init(B.s_issued, 1);
+    mbar_init(B.s_issued + 8, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -562,104 +591,139 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           wait_bar(B.slot_full + 8 * (k % NS), (k / NS) & 1, abort_flag, nullptr, false);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------- MMA issuers
+    // Warp 9 issues the MMAs of query tile 0, warp 10 those of query tile 1.
+    // Both walk the CTA's tile list in order; for position i an issuer does
+    //   PV_u(i-1) [needs P_u(i-1), V_{i-1}], then S_u(i) [needs K_i]
+    // S_u(i) overwrites the TMEM columns P_u(i-1) was read from; MMAs of one
+    // thread execute in order, so issuing it after PV_u(i-1) is enough.  Each
+    // issuer releases every K and V slot once: by a commit after its MMAs that
+    // read the slot, or -- for a tile its query tile does not reach -- by a
+    // plain arrive after the tile has landed (so no issuer can run a lap of
+    // the ring ahead of the other).
+    // The two query tiles are kept half a period apart (ping-pong): S_0(i) is
+    // issued after S_1(i-1), and S_1(i) after S_0(i), so the tensor core runs
+    // S_0(i), PV_1(i-1), S_1(i), PV_0(i), ... and each softmax warpgroup works
+    // while the other tile's MMAs execute.  (If Q_1 has no rows, issuer 1 is
+    // idle and issuer 0 skips the handshake.)
+    const int u = warp - 9;
+    const bool act = u ? w.active[1] : w.active[0];
+    if (lane == 0 && act) {
       bool ok = wait_bar(B.q_full, 0, abort_flag, p.err);
       tc_fence_after();
-      int armed[NS], readers[NS];
-      for (int i = 0; i < NS; ++i) armed[i] = -1, readers[i] = 0;
-      int len_u[2] = {seq_len(w, 0), seq_len(w, 1)};
-      int pv_count[2] = {0, 0};
       constexpr uint32_t kIdescS = idesc_bf16(kRows, kKeys, false);
       constexpr uint32_t kIdescSg = idesc_bf16(kRows, kGKeys, false);
       constexpr uint32_t kIdescPV = idesc_bf16(kRows, D, true);
+      const uint64_t dq = sw128_desc(s_q0 + u * C::kQBytes, 16, 1024);
+      const uint64_t dk_base = sw128_desc(s_slots, 16, 1024);
+      const uint64_t dv_band = sw128_desc(s_slots, kKeys * 128, 1024);   // LBO: next 64 columns of V
+      const uint64_t dv_glob = sw128_desc(s_slots, kGKeys * 128, 1024);
+      const uint32_t d_s = tmem + u * 128, d_o = tmem + 256 + u * 128;
+      const uint32_t s_full = B.s_full + 8 * u, p_full = B.p_full + 8 * u;
+      const int n_tiles = w.nb + w.ng;
+      const int a_u = (u ? w.n_lo[1] : w.n_lo[0]) - w.lo;
+      const int b_u = a_u + (u ? w.n_cnt[1] : w.n_cnt[0]);
+      const int last = w.ng > 0 ? n_tiles - 1 : b_u - 1;
+      int pv = 0;
+      int k_slot = 0, k_par = 0;  // ring position and phase of K_i (load 2i)
 
-      auto acquire = [&](int load) -> bool {
-        const int s = load % NS;
-        if (armed[s] != load) {
-          if (!wait_bar(B.slot_full + 8 * s, (load / NS) & 1, abort_flag, p.err)) return false;
-          tc_fence_after();
-          armed[s] = load;
-          readers[s] = readers_of(w, load >> 1);
-        }
-        return true;
-      };
-      auto release = [&](int load) {
-        const int s = load % NS;
-        if (--readers[s] == 0) mma_commit(B.slot_empty + 8 * s);
-      };
-      auto issue_s = [&](int u, int pos) -> bool {
-        const int load = 2 * pos;
-        if (!acquire(load)) return false;
-        const bool gt = pos >= w.nb;
-        const int rows = gt ? kGKeys : kKeys;
-        const uint32_t kbase = s_slots + (load % NS) * C::kSlotBytes;
-        const uint32_t qbase = s_q0 + u * C::kQBytes;
+      for (int i = 0; i <= n_tiles && ok; ++i) {
+        const int v_slot = k_slot == 0 ? NS - 1 : k_slot - 1;
+        const int v_par = k_slot == 0 ? k_par ^ 1 : k_par;
+        if (i > 0) {
+          const int ip = i - 1;
+          const bool gp = ip >= w.nb;
+          const bool reads = gp || (ip >= a_u && ip < b_u);
+          ok = wait_bar(B.slot_full + 8 * v_slot, v_par, abort_flag, p.err);
+          if (ok && reads) ok = wait_bar(p_full, pv & 1, abort_flag, p.err);
+          if (!ok) break;
+          if (reads) {
+            tc_fence_after();
+            const uint64_t off = (uint64_t)((v_slot * C::kSlotBytes) >> 4);
+            const uint32_t first = pv == 0 ? 0u : 1u;
+            if (!gp) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_q = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
-          const uint32_t off_k = (kk >> 2) * (rows * 128) + (kk & 3) * 32;
-          mma_ss(tmem + u * 128, sw128_desc(qbase + off_q, 16, 1024),
-                 sw128_desc(kbase + off_k, 16, 1024), gt ? kIdescSg : kIdescS, kk > 0);
+              for (int kk = 0; kk < kKeys / 16; ++kk)
+                mma_ts(d_o, d_s + kk * 8, dv_band + off + (uint64_t)(kk * 128), kIdescPV,
+                       kk > 0 ? 1u : first);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < kGKeys / 16; ++kk)
+                mma_ts(d_o, d_s + kk * 8, dv_glob + off + (uint64_t)(kk * 128), kIdescPV,
+                       kk > 0 ? 1u : first);
+            }
+            ++pv;
+            mma_commit(B.slot_empty + 8 * v_slot);
+            if (ip == last) mma_commit(B.o_final + 8 * u);
+          } else {
+            mbar_arrive(B.slot_empty + 8 * v_slot);
+          }
         }
-        mma_commit(B.s_full + 8 * u);
-        release(load);
-        return true;
-      };
-      auto issue_pv = [&](int u, int pos, bool last) -> bool {
-        if (!wait_bar(B.p_full + 8 * u, pv_count[u] & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const int load = 2 * pos + 1;
-        if (!acquire(load)) return false;
-        const bool gt = pos >= w.nb;
-        const int rows = gt ? kGKeys : kKeys;
-        const uint32_t vbase = s_slots + (load % NS) * C::kSlotBytes;
-        for (int kk = 0; kk < rows / 16; ++kk) {
-          mma_ts(tmem + 256 + u * 128, tmem + u * 128 + kk * 8,
-                 sw128_desc(vbase + kk * 16 * 128, rows * 128, 1024), kIdescPV,
-                 (pv_count[u] > 0 || kk > 0) ? 1u : 0u);
+        if (i < n_tiles) {
+          const bool gc = i >= w.nb;
+          const bool reads = gc || (i >= a_u && i < b_u);
+          ok = wait_bar(B.slot_full + 8 * k_slot, k_par, abort_flag, p.err);
+          // ping-pong handshake (position i of tile 1 follows position i of tile 0)
+          if (ok && w.active[1]) {
+            if (u == 1)
+              ok = wait_bar(B.s_issued, i & 1, abort_flag, p.err);
+            else if (i > 0)
+              ok = wait_bar(B.s_issued + 8, (i - 1) & 1, abort_flag, p.err);
+          }
+          if (!ok) break;
+          if (reads) {
+            tc_fence_after();
+            const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
+            if (!gc) {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                       dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                       dk + (((kk >> 2) * (kGKeys * 128) + (kk & 3) * 32) >> 4), kIdescSg, kk > 0);
+            }
+            mma_commit(s_full);
+            mma_commit(B.slot_empty + 8 * k_slot);
+          } else {
+            mbar_arrive(B.slot_empty + 8 * k_slot);
+          }
+          mbar_arrive(B.s_issued + 8 * u);  // S_u(i) issued (or not needed)
         }
-        ++pv_count[u];
-        release(load);
-        if (last) mma_commit(B.o_final + 8 * u);
-        return true;
-      };
-
-      int idx[2] = {0, 0};
-      for (int u = 0; u < 2 && ok; ++u)
-        if (len_u[u] > 0) ok = issue_s(u, seq_pos(w, u, 0));
-      while (ok && (idx[0] < len_u[0] || idx[1] < len_u[1])) {
-        for (int u = 0; u < 2 && ok; ++u) {
-          if (idx[u] >= len_u[u]) continue;
-          const int pos = seq_pos(w, u, idx[u]);
-          ++idx[u];
-          ok = issue_pv(u, pos, idx[u] == len_u[u]);
-          if (ok && idx[u] < len_u[u]) ok = issue_s(u, seq_pos(w, u, idx[u]));
+        k_slot += 2;  // advance by two loads (K_i, V_i)
+        if (k_slot >= NS) {
+          k_slot -= NS;
+          k_par ^= 1;
         }
       }
-      // everything issued has completed before TMEM is released
-      mma_commit(B.mma_done);
-      wait_bar(B.mma_done, 0, abort_flag, nullptr, false);
+      // everything this thread issued has completed before TMEM is released
+      mma_commit(B.mma_done + 8 * u);
+      wait_bar(B.mma_done + 8 * u, 0, abort_flag, nullptr, false);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------- softmax
+    // warpgroup u: one thread per row of query tile u
     const int u = warp >> 2;
     const int row = tid & 127;
-    const int wq = (tid & 127) >> 5;
-    const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+    const uint32_t lane_addr = (uint32_t)((row >> 5) * 32) << 16;
     const uint32_t t_s = tmem + lane_addr + u * 128;
     const uint32_t t_o = tmem + lane_addr + 256 + u * 128;
-    const int n = seq_len(w, u);
+    const bool act_u = u ? w.active[1] : w.active[0];
+    const int nlo_u = u ? w.n_lo[1] : w.n_lo[0];
+    const int ncnt_u = u ? w.n_cnt[1] : w.n_cnt[0];
+    const int n = act_u ? ncnt_u + w.ng : 0;
     const float sl = p.scale_log2;
     const int t_q = GLOBAL ? 0 : (w.q_tile + u) * kRows + row;  // class coordinate
-    const int64_t pos_q = GLOBAL ? 0 : (int64_t)w.r + (int64_t)w.d * t_q;
     const int half = p.half;
+    const int bar_id = 1 + u;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
 
     for (int i = 0; i < n && ok; ++i) {
-      const int pos = seq_pos(w, u, i);
+      const int pos = seq_pos_s(w, nlo_u, ncnt_u, i);
       const bool gt = pos >= w.nb;
       ok = __all_sync(0xffffffffu, wait_bar(B.s_full + 8 * u, i & 1, abort_flag, p.err));
       if (!ok) break;
@@ -679,12 +743,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           c_hi = min(t_q + half, w.len - 1) - kb;
         }
         softmax_tile<kKeys, D>(t_s, t_o, sl, full ? kMaskNone : kMaskInterval, c_lo, c_hi,
-                               nullptr, 0, 0, 0, false, m_run, l_run);
+                               nullptr, 0, 0, 0, 0, 1, false, m_run, l_run);
       } else {
         const int g0 = (pos - w.nb) * kGKeys;
         const bool dedup = (w.flags >> u) & 1;
         softmax_tile<kGKeys, D>(t_s, t_o, sl, kMaskGlobal, 0, p.n_g - 1 - g0, g_list, g0, t_q,
-                                half, dedup, m_run, l_run);
+                                half, w.r, w.d, dedup, m_run, l_run);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -696,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
       // every thread of the warpgroup takes part in the same barriers, so the
       // decision to write the tile is made jointly
       bool fin = ok && wait_bar(B.o_final + 8 * u, 0, abort_flag, p.err);
-      fin = named_bar_and(1 + u, 128, fin);
+      fin = named_bar_and(bar_id, 128, fin);
       if (fin) tc_fence_after();
       if (!GLOBAL) {
         // normalise, stage the bf16 tile in this query tile's (now idle) smem
@@ -722,11 +786,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
               *reinterpret_cast<uint4 *>(rowp + phys * 16) = v;
             }
           }
-          if (p.lse && t_q < w.len)
+          if (p.lse && t_q < w.len) {
+            const int64_t pos_q = (int64_t)w.r + (int64_t)w.d * t_q;
             p.lse[(int64_t)w.bh * p.N + pos_q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+          }
           fence_proxy_async_smem();
         }
-        named_bar_sync(1 + u, 128);
+        named_bar_sync(bar_id, 128);
         if (fin && row == 0) {
           const int ls = w.slot - P.slot_base;
           for (int h = 0; h < C::kHalves; ++h)
