@@ -73,6 +73,17 @@ def workload_flops(w, sa):
     return 4.0 * w.D * pairs, 4.0 * w.D * (pairs - global_pairs), pairs
 
 
+def rank_seed(w, rank: int) -> int:
+    """Seed of rank `rank`'s batch: rank 0 uses the workload's own seed, other
+    ranks independent batches of the same shape (weak scaling)."""
+    return 1000 + w.number + (7919 * rank if rank else 0)
+
+
+def job_value(flops_per_step: float, steps: int, ms_max: float, world: int) -> float:
+    """Whole-job TFLOP/s: work of all ranks over the slowest rank's time."""
+    return world * flops_per_step * steps / (ms_max * 1e-3) / 1e12
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -244,7 +255,7 @@ def run_ours(args):
     if args.heads:
         w = dataclasses.replace(w, H=args.heads, dilation=w.dilation[:1] * args.heads)
     # each rank runs its own independent batch of the workload (weak scaling)
-    qkv = inputs.draw_qkv(w, seed=(1000 + w.number) if rank == 0 else (1000 + w.number + 7919 * rank))
+    qkv = inputs.draw_qkv(w, seed=rank_seed(w, rank))
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
 
     def host_tensor(a):
@@ -283,7 +294,7 @@ def run_ours(args):
     sa.sync_status(stream)
     ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_step = ms_total / args.steps
-    value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+    value = job_value(flops_step, args.steps, ms_total, world)
 
     pk = peaks()
     band_ms = prof["band"]["ms"] / max(1, prof["band"]["launches"])
