@@ -4,25 +4,36 @@
 // What one CTA computes (Unlimiformer section 2.3 Eq. (1) under the additive
 // {0,-inf} mask of GMAT's "Global-Memory Augmented Transformers" section):
 // two 128-row query tiles Q_0, Q_1, each against its own list of key tiles --
-// the band tiles that intersect its rows' windows (Longformer glossary, "How the
-// Longformer attention works": sliding / dilated window) followed by the
-// gathered global keys (the same section's global attention; GMAT "Global
-// Memory") -- with an exact online softmax in fp32:
+// the gathered global keys (Longformer glossary, "How the Longformer attention
+// works": global attention; GMAT "Global Memory") followed by the band tiles
+// that intersect its rows' windows (the same section's sliding / dilated
+// window) -- with an exact online softmax in fp32.  The global tiles come first
+// because both query tiles read them: the two tiles' MMAs overlap from the
+// start of an item, and the next item's first loads depend only on slots the
+// current item released early.
 //
 //   S = Q_u K_j^T (tcgen05, fp32 in TMEM) -> scale, mask (edge tiles only),
 //   running max / sum per row -> P = exp2(S - m) as bf16 written back into the
-//   same TMEM columns -> O_u += P V_j (tcgen05, A operand from TMEM).
+//   same TMEM columns, in two halves -> O_u += P V_j (tcgen05, A operand from
+//   TMEM; the first half of the product starts once the first half of P is in
+//   place).
 //
 // In global mode the two query tiles are the gathered global rows and the key
 // tiles one chunk of all N keys; the CTA writes unnormalised partial outputs
 // and their (max, sum) for the merge kernel.
 //
-// Warp roles (352 threads): warps 0-3 softmax of Q_0 (one thread per row),
-// warps 4-7 softmax of Q_1, warp 8 TMA producer, warp 9 MMA issuer of Q_0 (and
-// TMEM allocator), warp 10 MMA issuer of Q_1.  TMEM: S_0 cols [0,128), S_1 [128,256), O_0 [256,256+D),
-// O_1 [384,384+D).  Shared memory: Q_0, Q_1, then a ring of key/value slots
-// (one K or V tile each), then barriers.  All tiles use the 128-byte swizzle
-// that TMA writes and the UMMA descriptors read.
+// The kernel is persistent: one CTA per SM walks the launch's work items with
+// a grid stride, keeping its barriers, TMEM and key/value ring across items,
+// so the next item's Q load and first MMAs overlap the current item's tail.
+//
+// Warp roles (352 threads): warps 0-3 softmax of Q_0 (one thread per row; they
+// also write the finished rows), warps 4-7 softmax of Q_1, warp 8 TMA producers
+// (lane 0 keys/values, lane 1 queries), warp 9 MMA issuer of Q_0 (and TMEM
+// allocator), warp 10 MMA issuer of Q_1.  TMEM: S_0 cols [0,128), S_1 [128,256), O_0
+// [256,256+D), O_1 [384,384+D).  Shared memory: two query-tile buffers (used
+// alternately, so the next item's Q_0 can land while Q_1 is still in use),
+// then a ring of key/value slots (one K or V tile each), then barriers.  All tiles use the
+// 128-byte swizzle that TMA writes and the UMMA descriptors read.
 //
 // Every wait on an mbarrier is bounded: after kWaitLimitNs the waiting thread
 // sets the CTA's abort flag and the device error word, and every role winds
@@ -44,7 +55,7 @@
 namespace sa {
 namespace tc {
 
-constexpr int kThreads = 352;     // eleven warps: 168 registers per thread
+constexpr int kThreads = 352;     // eleven warps (three on some sub-partitions): 168 registers
 constexpr int kRows = 128;         // query rows per tile (TMEM lanes)
 constexpr int kKeys = 128;         // keys per band tile
 constexpr int kGKeys = 64;         // keys per global tile
@@ -52,6 +63,11 @@ constexpr int kMaxSlotsPerLaunch = 16;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
 constexpr int kFarAway = -(1 << 30);  // class coordinate of a global outside the class
+constexpr bool kGlobalsFirst = false;  // global key tiles before (or after) the band tiles
+// Output tiles: staged in the tile's query buffer and written by TMA (the
+// buffer is released by the epilogue), or written from registers (the buffer
+// is released by the tile's last S MMA).
+constexpr bool kStagedStore = true;
 
 struct Maps {
   CUtensorMap q[kMaxSlotsPerLaunch], k[kMaxSlotsPerLaunch], v[kMaxSlotsPerLaunch],
@@ -66,6 +82,7 @@ struct Params {
   DevProblem p;
   int slot_base;    // slot index held in maps.q[0]
   int item_offset;  // first work item of this launch
+  int n_items;      // work items of this launch (CTAs stride over them)
 };
 
 template <int D>
@@ -76,9 +93,10 @@ struct Cfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kAux = 3072;  // barriers, flags, global positions (class coordinates)
   static constexpr int kSmemMax = 232448;
-  static constexpr int kSlots0 = (kSmemMax - 2 * kQBytes - kAux) / kSlotBytes;
+  static constexpr int kQBufs = 2;   // query tiles alternate between two buffers
+  static constexpr int kSlots0 = (kSmemMax - kQBufs * kQBytes - kAux) / kSlotBytes;
   static constexpr int kSlots = kSlots0 > 12 ? 12 : kSlots0;
-  static constexpr int kSmemBytes = 2 * kQBytes + kSlots * kSlotBytes + kAux;
+  static constexpr int kSmemBytes = kQBufs * kQBytes + kSlots * kSlotBytes + kAux;
   static_assert(kSlots >= 4, "the key/value ring needs at least four slots");
 };
 
@@ -105,6 +123,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "{\n"
       ".reg .pred p;\n"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking check of a barrier phase.  Several polls issued back to back
+// overlap their latency (~80 cycles each), unlike a chain of waits.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       "selp.u32 %0, 1, 0, p;\n"
       "}\n"
       : "=r"(ok)
@@ -156,12 +189,19 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
-__device__ __forceinline__ void tma_store_commit_and_drain() {
+// Commit the issued bulk stores and wait until they have read shared memory.
+__device__ __forceinline__ void tma_store_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
 }
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -224,6 +264,55 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Issue forms for a converged warp: elect.sync picks one lane, which issues the
+// tcgen05 operation (a converged warp with warp-uniform operands issues MMAs at
+// about twice the rate of a single diverged lane).
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p, e;\n"
+      ".reg .b32 r;\n"
+      "elect.sync r|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p, e;\n"
+      ".reg .b32 r;\n"
+      "elect.sync r|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n"
+      ".reg .pred e;\n"
+      ".reg .b32 r;\n"
+      "elect.sync r|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "}\n" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  asm volatile(
+      "{\n"
+      ".reg .pred e;\n"
+      ".reg .b32 r;\n"
+      "elect.sync r|e, 0xffffffff;\n"
+      "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n"
+      "}\n" ::"r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)
@@ -282,14 +371,15 @@ struct Work {
   int key0;      // global mode: first key of the chunk
   int key_end;   // global mode: one past the chunk's last key
   int chunk;
+  int g_tile;    // global mode: pair of 128-row tiles of the gathered global rows
 };
 
 template <bool GLOBAL>
-__device__ __forceinline__ Work make_work(const Params &P) {
+__device__ __forceinline__ Work make_work(const Params &P, int item) {
   Work w{};
   const DevProblem &p = P.p;
   if (!GLOBAL) {
-    const BandItem it = p.band[P.item_offset + blockIdx.x];
+    const BandItem it = p.band[P.item_offset + item];
     const Slot sl = p.slots[it.slot];
     w.bh = it.bh;
     w.slot = it.slot;
@@ -309,9 +399,10 @@ __device__ __forceinline__ Work make_work(const Params &P) {
     w.nb = hi - w.lo + 1;
     w.ng = (p.n_g + kGKeys - 1) / kGKeys;
   } else {
-    const GlobalItem it = p.gitems[blockIdx.x];
+    const GlobalItem it = p.gitems[item];
     w.bh = it.bh;
     w.chunk = it.chunk;
+    w.g_tile = it.g_tile;
     w.key0 = it.chunk * p.chunk_len;
     w.key_end = min(p.N, w.key0 + p.chunk_len);
     w.lo = 0;
@@ -326,50 +417,62 @@ __device__ __forceinline__ Work make_work(const Params &P) {
   return w;
 }
 
+// First row of query tile u in its tensor map (class coordinate, or row of the
+// gathered global rows).
+template <bool GLOBAL>
+__device__ __forceinline__ int q_row_of(const Work &w, int u) {
+  return GLOBAL ? (w.g_tile * 2 + u) * kRows : (w.q_tile + u) * kRows;
+}
+template <bool GLOBAL>
+__device__ __forceinline__ const CUtensorMap *map_q_of(const Params &P, const Work &w) {
+  return GLOBAL ? &P.maps.qg : &P.maps.q[w.slot - P.slot_base];
+}
+
 // Position in the CTA's tile list of the i-th tile of a query tile whose band
 // tiles start at n_lo (n_cnt of them).
 __device__ __forceinline__ int seq_pos_s(const Work &w, int n_lo, int n_cnt, int i) {
+  if (kGlobalsFirst) return i < w.ng ? i : w.ng + (n_lo - w.lo) + (i - w.ng);
   return i < n_cnt ? (n_lo - w.lo + i) : (w.nb + (i - n_cnt));
 }
-// Position in the CTA's tile list of the i-th tile of query tile u.
-__device__ __forceinline__ int seq_pos(const Work &w, int u, int i) {
-  return i < w.n_cnt[u] ? (w.n_lo[u] - w.lo + i) : (w.nb + (i - w.n_cnt[u]));
+// Is position pos of the item's tile list a global tile, and which band tile
+// (or global tile) is it?
+__device__ __forceinline__ bool is_global_pos(const Work &w, int pos) {
+  return kGlobalsFirst ? pos < w.ng : pos >= w.nb;
+}
+__device__ __forceinline__ int band_index(const Work &w, int pos) {
+  return kGlobalsFirst ? pos - w.ng : pos;
+}
+__device__ __forceinline__ int global_index(const Work &w, int pos) {
+  return kGlobalsFirst ? pos : pos - w.nb;
 }
 __device__ __forceinline__ int seq_len(const Work &w, int u) {
   return w.active[u] ? w.n_cnt[u] + w.ng : 0;
 }
 struct Bars {
   uint32_t slot_full, slot_empty;  // arrays of kSlots
-  uint32_t q_full, s_full, p_full, o_final, mma_done, s_issued;
+  uint32_t q_full, q_empty;  // arrays of kQBufs
+  uint32_t s_full, p_half, p_full, o_final, mma_done, s_issued;  // arrays of 2
 };
 
 // ---------------------------------------------------------------------------
 // softmax: one key tile of W columns for one row
 
-template <int W>
-struct TileScores {
-  float s[W];
-};
-
-// One key tile of W columns for one query row (this thread's TMEM lane):
-// load S, mask, update the running maximum (rescaling O in TMEM when the
-// reference maximum moves), write P = 2^(scale*S - m) as bf16 over S, and add
-// its row sum.  Scores stay in base-2 units: scale is scale*log2(e).
-//   mask_mode 0: no mask.  1: keep columns [c_lo, c_hi].  2: global tile --
-//   keep columns <= c_hi whose global position is not already in the row's band.
 enum { kMaskNone = 0, kMaskInterval = 1, kMaskGlobal = 2 };
 
-// W scores of this thread's row from TMEM, scaled (negative scales only: a
-// positive scale is folded into the exponent) and masked to -inf.
-//   mask_mode 0: no mask.  1: keep columns [c_lo, c_hi].  2: global keys --
-//   keep columns <= c_hi whose global position is not already in the row's band
-//   (globals[g0 + x] is the global's class coordinate t_g, or kFarAway; the row
-//   is class position t_q, and the global is in its band when |t_q - t_g| <= half).
+// Masking of one key tile's scores (scores are in base-2 units; a negative
+// scale is applied to the scores themselves so that the maximum is taken on
+// scaled scores, a positive one is folded into the exponent):
+//   mode kMaskNone: every column.  kMaskInterval: columns [c_lo, c_hi].
+//   kMaskGlobal: columns <= c_hi whose global position is not already in the
+//   row's band (globals[g0 + x] is the global's class coordinate t_g, or
+//   kFarAway; the row is class position t_q; the global is in the row's band
+//   when |t_q - t_g| <= half, and is then counted once, as a band key).
+
+// W scores of this thread's row from TMEM, scaled and masked to -inf.
 template <int W>
-__device__ __forceinline__ void load_scores(uint32_t t_s, float scale, int mask_mode, int c_lo,
-                                            int c_hi, const int32_t *globals, int g0, int t_q,
-                                            int half, int cls_r, int cls_d, bool dedup,
-                                            float (&s)[W]) {
+__device__ __forceinline__ void load_scores(uint32_t t_s, float neg_scale, int mode, int c_lo, int c_hi,
+                                            const int32_t *globals, int g0, int t_q, int half,
+                                            bool dedup, float (&s)[W]) {
   {
     uint32_t r[W];
     if constexpr (W == 128)
@@ -381,15 +484,17 @@ __device__ __forceinline__ void load_scores(uint32_t t_s, float scale, int mask_
 #pragma unroll
     for (int x = 0; x < W; ++x) s[x] = __uint_as_float(r[x]);
   }
-  if (scale < 0.f) {  // general path: scale first so that the maximum is taken on scaled scores
+  if (neg_scale < 0.f) {
 #pragma unroll
-    for (int x = 0; x < W; ++x) s[x] *= scale;
+    for (int x = 0; x < W; ++x) s[x] *= neg_scale;
   }
-  if (mask_mode == kMaskInterval) {
+  // band tiles (kKeys wide) take the interval mask, global tiles (kGKeys
+  // wide) the global one
+  if (W == kKeys && mode == kMaskInterval) {
 #pragma unroll
     for (int x = 0; x < W; ++x)
       if (x < c_lo || x > c_hi) s[x] = -INFINITY;
-  } else if (mask_mode == kMaskGlobal) {
+  } else if (W == kGKeys && mode == kMaskGlobal) {
 #pragma unroll
     for (int x = 0; x < W; ++x) {
       bool valid = x <= c_hi;
@@ -402,22 +507,22 @@ __device__ __forceinline__ void load_scores(uint32_t t_s, float scale, int mask_
   }
 }
 
-// One key tile of W columns for one query row (this thread's TMEM lane):
-// P = 2^(scale*S - m) as bf16 written over S, running maximum m and row sum l
-// updated, O in TMEM rescaled when the reference maximum moves.  Scores are in
-// base-2 units (scale = scale*log2(e)).  The reference maximum is raised only
-// when the tile maximum exceeds it by more than 2^8, so O is rescaled rarely;
-// the same reference is used for P and for the running sum, so the result is
-// exact either way.
+// One key tile of W columns for one query row (this thread's TMEM lane): P =
+// 2^(scale*S - m) as bf16 written over S, running maximum m and row sum l
+// updated, O in TMEM rescaled when the reference maximum moves.  The reference
+// maximum is raised only when the tile maximum exceeds it by more than 2^8, so
+// O is rescaled rarely; the same reference is used for P and for the running
+// sum, so the result is exact either way.  A 128-key tile is written in two
+// halves and announces the first (keys 0-63) on bar_half, so that the first
+// half of P V can start while the second half of P is computed.
 template <int W, int D>
-__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float scale,
-                                             int mask_mode, int c_lo, int c_hi,
-                                             const int32_t *globals, int g0, int t_q, int half,
-                                             int cls_r, int cls_d, bool dedup, float &m_run,
-                                             float &l_run) {
+__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float scale, int mode,
+                                             int c_lo, int c_hi, const int32_t *globals, int g0,
+                                             int t_q, int half, bool dedup, uint32_t bar_half,
+                                             int lane, float &m_run, float &l_run) {
   const float scl = scale < 0.f ? 1.f : scale;
   float s[W];
-  load_scores<W>(t_s, scale, mask_mode, c_lo, c_hi, globals, g0, t_q, half, cls_r, cls_d, dedup, s);
+  load_scores<W>(t_s, scale < 0.f ? scale : 0.f, mode, c_lo, c_hi, globals, g0, t_q, half, dedup, s);
   // row maximum: eight chains of three-input max
   float mx[8];
 #pragma unroll
@@ -432,6 +537,20 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
   const float m_new = need ? mt : m_run;
   const float alpha = need ? ex2(m_run - m_new) : 1.f;
   const bool rescale = need && m_run != -INFINITY;  // O holds earlier tiles of this row
+  if (__any_sync(0xffffffffu, rescale)) {
+    // O holds the previous tiles (their PV was issued before this tile's S,
+    // whose completion has been observed); bring it to the new reference
+    // before any of this tile's P can be multiplied into it
+    const float a = rescale ? alpha : 1.f;
+#pragma unroll 1
+    for (int c = 0; c < D / 16; ++c) {
+      uint32_t r[16];
+      tmem_ld16(t_o + c * 16, r);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * a);
+      tmem_st16(t_o + c * 16, r);
+    }
+  }
   // P: the argument two columns at a time (packed fp32x2 FMA), the exponential
   // on the SFU, row sums in four packed accumulators
   const float neg = (m_new == -INFINITY) ? 0.f : -m_new;
@@ -439,37 +558,32 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
   float2 sum2[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
-  {
-    uint32_t pr[W / 2];
 #pragma unroll
-    for (int i = 0; i < W / 2; ++i) {
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t pr[W / 4];
+#pragma unroll
+    for (int j = 0; j < W / 4; ++j) {
+      const int i = hh * (W / 4) + j;
       const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
       const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
       sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
-      pr[i] = pack_bf16(e.x, e.y);
+      pr[j] = pack_bf16(e.x, e.y);
     }
     if constexpr (W == 128)
-      tmem_st64(t_s, pr);
+      tmem_st32(t_s + hh * 32, pr);
     else
-      tmem_st32(t_s, pr);
+      tmem_st16(t_s + hh * 16, pr);
+    if (W == 128 && hh == 0) {
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_half);
+    }
   }
   const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
   const float2 s4 = __fadd2_rn(s01, s23);
   l_run = (need ? l_run * alpha : l_run) + (s4.x + s4.y);
   m_run = m_new;
-  if (__any_sync(0xffffffffu, rescale)) {
-    // O holds the previous tiles (their PV was issued before this tile's S,
-    // whose completion has been observed); bring it to the new reference
-    const float a = rescale ? alpha : 1.f;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(t_o + c * 32, r);
-#pragma unroll
-      for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * a);
-      tmem_st32(t_o + c * 32, r);
-    }
-  }
 }
 
 template <int D, bool GLOBAL>
@@ -479,22 +593,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw;
   const uint32_t s_q0 = smem_u32(smem);
-  const uint32_t s_slots = s_q0 + 2 * C::kQBytes;
-  uint8_t *aux = smem + 2 * C::kQBytes + NS * C::kSlotBytes;
-  uint64_t *bar_mem = reinterpret_cast<uint64_t *>(aux);  // 2*NS + 12 barriers
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(aux + 8 * (2 * NS + 12));
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(aux + 8 * (2 * NS + 12) + 4);
-  int32_t *g_list = reinterpret_cast<int32_t *>(aux + 1024);  // SA_MAX_GLOBALS entries
-  static_assert(8 * (2 * NS + 12) + 16 <= 1024 && 1024 + 4 * SA_MAX_GLOBALS <= C::kAux, "aux layout");
+  constexpr int NQ = C::kQBufs;
+  const uint32_t s_slots = s_q0 + NQ * C::kQBytes;
+  uint8_t *aux = smem + NQ * C::kQBytes + NS * C::kSlotBytes;
+  constexpr int kBars = 2 * NS + 2 * NQ + 12;
+  uint64_t *bar_mem = reinterpret_cast<uint64_t *>(aux);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(aux + 8 * kBars);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(aux + 8 * kBars + 4);
+  int32_t *g_lists = reinterpret_cast<int32_t *>(aux + 1024);  // [2][SA_MAX_GLOBALS]
+  static_assert(8 * kBars + 16 <= 1024 && 1024 + 8 * SA_MAX_GLOBALS <= C::kAux, "aux layout");
   Bars B;
   B.slot_full = smem_u32(bar_mem);
   B.slot_empty = B.slot_full + 8 * NS;
-  B.q_full = B.slot_empty + 8 * NS;
-  B.s_full = B.q_full + 8;   // [2]
-  B.p_full = B.s_full + 16;  // [2]
-  B.o_final = B.p_full + 16; // [2]
-  B.mma_done = B.o_final + 16;  // [2]
-  B.s_issued = B.mma_done + 16; // [2]
+  B.q_full = B.slot_empty + 8 * NS;  // [NQ]
+  B.q_empty = B.q_full + 8 * NQ;     // [NQ]
+  B.s_full = B.q_empty + 8 * NQ;     // [2]
+  B.p_half = B.s_full + 16;          // [2]
+  B.p_full = B.p_half + 16;          // [2]
+  B.o_final = B.p_full + 16;         // [2]
+  B.mma_done = B.o_final + 16;       // [2]
+  B.s_issued = B.mma_done + 16;      // [2]
 
   const DevProblem &p = P.p;
   const int tid = threadIdx.x;
@@ -503,33 +621,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     return;
   }
   const int warp = tid >> 5, lane = tid & 31;
-  const Work w = make_work<GLOBAL>(P);
+  const int n_items = P.n_items;
+  const int item0 = blockIdx.x, stride = gridDim.x;
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(B.slot_full + 8 * i, 1);
-      mbar_init(B.slot_empty + 8 * i, w.active[1] ? 2 : 1);  // one arrival per issuing warp
+      mbar_init(B.slot_empty + 8 * i, 2);  // one arrival per MMA issuer
     }
-    mbar_init(B.q_full, 1);
+    for (int b = 0; b < NQ; ++b) {
+      mbar_init(B.q_full + 8 * b, 1);
+      mbar_init(B.q_empty + 8 * b, 1);
+    }
     for (int u = 0; u < 2; ++u) {
       mbar_init(B.s_full + 8 * u, 1);
-      mbar_init(B.p_full + 8 * u, 4);  // one arrival per softmax warp of the tile's warpgroup
+      mbar_init(B.p_half + 8 * u, 4);  // one arrival per softmax warp of the tile's warpgroup
+      mbar_init(B.p_full + 8 * u, 4);
       mbar_init(B.o_final + 8 * u, 1);
+      mbar_init(B.mma_done + 8 * u, 1);
+      mbar_init(B.s_issued + 8 * u, 1);
     }
-    mbar_init(B.mma_done, 1);
-    mbar_init(B.mma_done + 8, 1);
-    mbar_init(B.s_issued, 1);
-    mbar_init(B.s_issued + 8, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (!GLOBAL) {
-    // global positions in this CTA's residue-class coordinates: g = r + d*t
-    // gives t; a global outside the class can never lie in a row's band
-    for (int i = tid; i < p.n_g; i += kThreads) {
-      const int g = p.globals[i] - w.r;
-      g_list[i] = (g >= 0 && g % w.d == 0) ? g / w.d : kFarAway;
-    }
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -540,49 +653,75 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const CUtensorMap *map_q, *map_k, *map_v;
-  if (!GLOBAL) {
-    const int ls = w.slot - P.slot_base;
-    map_q = &P.maps.q[ls];
-    map_k = &P.maps.k[ls];
-    map_v = &P.maps.v[ls];
-  } else {
-    map_q = &P.maps.qg;
-    map_k = &P.maps.kp;
-    map_v = &P.maps.vp;
-  }
-
-  if (warp == 8) {
-    // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      const int n_active = (int)w.active[0] + (int)w.active[1];
-      mbar_expect_tx(B.q_full, n_active * C::kQBytes);
-      for (int u = 0; u < 2; ++u) {
-        if (!w.active[u]) continue;
-        const int y = GLOBAL ? u * kRows : (w.q_tile + u) * kRows;
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_3d(s_q0 + u * C::kQBytes + h * (kRows * 128), map_q, B.q_full, 64 * h, y, w.bh);
-      }
-      const int n_tiles = w.nb + w.ng;
-      int n = 0;
+  if (warp == 8 && lane == 1) {
+    // ------------------------------------------------------------- Q producer
+    // Query tiles are loaded in order (item by item, tile 0 then tile 1) into
+    // the buffers 0, 1, 0, 1, ...; a buffer is refilled once the output tile
+    // staged in it has been stored.  The following item's query rows are
+    // prefetched into L2.
+    {
+      uint32_t j = 0;  // query tiles loaded so far
       bool ok = true;
-      for (int pos = 0; pos < n_tiles && ok; ++pos) {
-        const bool gt = pos >= w.nb;
-        const int rows = gt ? kGKeys : kKeys;
-        const int y = gt ? (pos - w.nb) * kGKeys : (GLOBAL ? w.key0 + pos * kKeys : (w.lo + pos) * kKeys);
-        const CUtensorMap *mk = gt ? &P.maps.kg : map_k;
-        const CUtensorMap *mv = gt ? &P.maps.vg : map_v;
-        for (int which = 0; which < 2 && ok; ++which, ++n) {
-          const int s = n % NS, use = n / NS;
-          if (!wait_bar(B.slot_empty + 8 * s, (use & 1) ^ 1, abort_flag, p.err)) {
+      for (int item = item0; item < n_items && ok; item += stride) {
+        const Work w = make_work<GLOBAL>(P, item);
+        if (item + stride < n_items) {
+          const Work wn = make_work<GLOBAL>(P, item + stride);
+          const CUtensorMap *mq = map_q_of<GLOBAL>(P, wn);
+          for (int u = 0; u < 2; ++u)
+            if (wn.active[u])
+              for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(mq, 64 * h, q_row_of<GLOBAL>(wn, u), wn.bh);
+        }
+        const CUtensorMap *mq = map_q_of<GLOBAL>(P, w);
+        for (int u = 0; u < 2 && ok; ++u) {
+          if (!w.active[u]) continue;
+          const uint32_t b = j % NQ, use = j / NQ;
+          if (!wait_bar(B.q_empty + 8 * b, (use & 1u) ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          const uint32_t dst = s_slots + s * C::kSlotBytes;
-          mbar_expect_tx(B.slot_full + 8 * s, rows * D * 2);
+          mbar_expect_tx(B.q_full + 8 * b, C::kQBytes);
           for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(dst + h * (rows * 128), which ? mv : mk, B.slot_full + 8 * s, 64 * h, y,
-                        w.bh);
+            tma_load_3d(s_q0 + b * C::kQBytes + h * (kRows * 128), mq, B.q_full + 8 * b, 64 * h,
+                        q_row_of<GLOBAL>(w, u), w.bh);
+          ++j;
+        }
+      }
+      if (!ok) {
+        // the last loads may still be in flight: let them land
+        for (uint32_t x = j > (uint32_t)NQ ? j - NQ : 0u; x < j; ++x)
+          wait_bar(B.q_full + 8 * (x % NQ), (x / NQ) & 1u, abort_flag, nullptr, false);
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------- K/V producer
+    // (lane 0; lane 1 of this warp is the Q producer, waiting independently)
+    if (lane == 0) {
+      int n = 0;
+      bool ok = true;
+      for (int item = item0; item < n_items && ok; item += stride) {
+        const Work w = make_work<GLOBAL>(P, item);
+        const CUtensorMap *map_k = GLOBAL ? &P.maps.kp : &P.maps.k[w.slot - P.slot_base];
+        const CUtensorMap *map_v = GLOBAL ? &P.maps.vp : &P.maps.v[w.slot - P.slot_base];
+        const int n_tiles = w.nb + w.ng;
+        for (int pos = 0; pos < n_tiles && ok; ++pos) {
+          const bool gt = is_global_pos(w, pos);
+          const int bp = band_index(w, pos);
+          const int rows = gt ? kGKeys : kKeys;
+          const int y = gt ? global_index(w, pos) * kGKeys : (GLOBAL ? w.key0 + bp * kKeys : (w.lo + bp) * kKeys);
+          const CUtensorMap *mk = gt ? &P.maps.kg : map_k;
+          const CUtensorMap *mv = gt ? &P.maps.vg : map_v;
+          for (int which = 0; which < 2; ++which, ++n) {
+            const int s = n % NS, use = n / NS;
+            if (!wait_bar(B.slot_empty + 8 * s, (use & 1) ^ 1, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = s_slots + s * C::kSlotBytes;
+            mbar_expect_tx(B.slot_full + 8 * s, rows * D * 2);
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_3d(dst + h * (rows * 128), which ? mv : mk, B.slot_full + 8 * s, 64 * h, y,
+                          w.bh);
+          }
         }
       }
       if (!ok) {
@@ -594,113 +733,144 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
   } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------- MMA issuers
     // Warp 9 issues the MMAs of query tile 0, warp 10 those of query tile 1.
-    // Both walk the CTA's tile list in order; for position i an issuer does
+    // Both walk every item's tile list in order; for position i an issuer does
     //   PV_u(i-1) [needs P_u(i-1), V_{i-1}], then S_u(i) [needs K_i]
     // S_u(i) overwrites the TMEM columns P_u(i-1) was read from; MMAs of one
     // thread execute in order, so issuing it after PV_u(i-1) is enough.  Each
     // issuer releases every K and V slot once: by a commit after its MMAs that
-    // read the slot, or -- for a tile its query tile does not reach -- by a
-    // plain arrive after the tile has landed (so no issuer can run a lap of
-    // the ring ahead of the other).
-    // The two query tiles are kept half a period apart (ping-pong): S_0(i) is
-    // issued after S_1(i-1), and S_1(i) after S_0(i), so the tensor core runs
-    // S_0(i), PV_1(i-1), S_1(i), PV_0(i), ... and each softmax warpgroup works
-    // while the other tile's MMAs execute.  (If Q_1 has no rows, issuer 1 is
-    // idle and issuer 0 skips the handshake.)
+    // read the slot, or -- for a tile its query tile does not reach, or an
+    // item whose query tile u is empty -- by a plain arrive after the tile has
+    // landed (so no issuer can run a lap of the ring ahead of the other).
+    // The two query tiles are kept half a period apart (ping-pong): S_0(g) is
+    // issued after S_1(g-1), and S_1(g) after S_0(g), counting positions g over
+    // all items of the CTA, so the tensor core runs S_0(g), PV_1(g-1), S_1(g),
+    // PV_0(g), ... and each softmax warpgroup works while the other tile's MMAs
+    // execute.
     const int u = warp - 9;
-    const bool act = u ? w.active[1] : w.active[0];
-    if (lane == 0 && act) {
-      bool ok = wait_bar(B.q_full, 0, abort_flag, p.err);
-      tc_fence_after();
+    {
       constexpr uint32_t kIdescS = idesc_bf16(kRows, kKeys, false);
       constexpr uint32_t kIdescSg = idesc_bf16(kRows, kGKeys, false);
       constexpr uint32_t kIdescPV = idesc_bf16(kRows, D, true);
-      const uint64_t dq = sw128_desc(s_q0 + u * C::kQBytes, 16, 1024);
       const uint64_t dk_base = sw128_desc(s_slots, 16, 1024);
       const uint64_t dv_band = sw128_desc(s_slots, kKeys * 128, 1024);   // LBO: next 64 columns of V
       const uint64_t dv_glob = sw128_desc(s_slots, kGKeys * 128, 1024);
       const uint32_t d_s = tmem + u * 128, d_o = tmem + 256 + u * 128;
       const uint32_t s_full = B.s_full + 8 * u, p_full = B.p_full + 8 * u;
-      const int n_tiles = w.nb + w.ng;
-      const int a_u = (u ? w.n_lo[1] : w.n_lo[0]) - w.lo;
-      const int b_u = a_u + (u ? w.n_cnt[1] : w.n_cnt[0]);
-      const int last = w.ng > 0 ? n_tiles - 1 : b_u - 1;
-      int pv = 0;
-      int k_slot = 0, k_par = 0;  // ring position and phase of K_i (load 2i)
-
-      for (int i = 0; i <= n_tiles && ok; ++i) {
-        const int v_slot = k_slot == 0 ? NS - 1 : k_slot - 1;
-        const int v_par = k_slot == 0 ? k_par ^ 1 : k_par;
-        if (i > 0) {
+      uint32_t pv = 0, jq = 0, g = 0;  // jq: query tiles of earlier items
+      int k_slot = 0, k_par = 0;  // ring position and phase of the next K load
+      bool ok = true;
+      for (int item = item0; item < n_items && ok; item += stride) {
+        const Work w = make_work<GLOBAL>(P, item);
+        const bool act = u ? w.active[1] : w.active[0];
+        const uint32_t jt = jq + ((u == 1 && w.active[0]) ? 1u : 0u);  // this tile's load index
+        jq += (uint32_t)w.active[0] + (uint32_t)w.active[1];
+        const uint32_t qb = jt % NQ;
+        const uint64_t dq = sw128_desc(s_q0 + qb * C::kQBytes, 16, 1024);
+        if (act) {
+          ok = __all_sync(0xffffffffu, wait_bar(B.q_full + 8 * qb, (jt / NQ) & 1u, abort_flag, p.err));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const int n_tiles = w.nb + w.ng;
+        const int a_u = (u ? w.n_lo[1] : w.n_lo[0]) - w.lo;
+        const int b_u = a_u + (u ? w.n_cnt[1] : w.n_cnt[0]);
+        // last position the tile reads
+        const int last = kGlobalsFirst ? w.ng + b_u - 1 : (w.ng > 0 ? n_tiles - 1 : b_u - 1);
+        int pv_item = 0;
+        for (int i = 0; i <= n_tiles && ok; ++i) {
+          const int v_slot = k_slot == 0 ? NS - 1 : k_slot - 1;
+          const int v_par = k_slot == 0 ? k_par ^ 1 : k_par;
+          const bool do_pv = i > 0, do_s = i < n_tiles;
           const int ip = i - 1;
-          const bool gp = ip >= w.nb;
-          const bool reads = gp || (ip >= a_u && ip < b_u);
-          ok = wait_bar(B.slot_full + 8 * v_slot, v_par, abort_flag, p.err);
-          if (ok && reads) ok = wait_bar(p_full, pv & 1, abort_flag, p.err);
-          if (!ok) break;
-          if (reads) {
-            tc_fence_after();
-            const uint64_t off = (uint64_t)((v_slot * C::kSlotBytes) >> 4);
-            const uint32_t first = pv == 0 ? 0u : 1u;
-            if (!gp) {
+          const bool gp = is_global_pos(w, ip), gc = is_global_pos(w, i);
+          const int ipb = band_index(w, ip), ib = band_index(w, i);
+          const bool pv_reads = do_pv && act && (gp || (ipb >= a_u && ipb < b_u));
+          const bool s_reads = do_s && act && (gc || (ib >= a_u && ib < b_u));
+          // ping-pong handshake (position g of tile 1 follows position g of tile 0)
+          const bool hs = do_s && (u == 1 || g > 0);
+          const uint32_t hs_bar = u == 1 ? B.s_issued : B.s_issued + 8;
+          const uint32_t hs_par = u == 1 ? (g & 1u) : ((g - 1) & 1u);
+          // the slot and handshake conditions are usually met already: poll
+          // them together, block only on P, and wait for what was not met
+          uint32_t pend = 0;
+          if (do_pv && !mbar_test(B.slot_full + 8 * v_slot, v_par)) pend |= 1u;
+          if (do_s && !mbar_test(B.slot_full + 8 * k_slot, k_par)) pend |= 2u;
+          if (hs && !mbar_test(hs_bar, hs_par)) pend |= 4u;
+          pend = __reduce_or_sync(0xffffffffu, pend);
+          if (do_pv) {
+            // a band tile's P arrives in two halves (keys 0-63, then 64-127)
+            if (pv_reads)
+              ok = __all_sync(0xffffffffu, wait_bar(gp ? p_full : B.p_half + 8 * u, pv & 1u, abort_flag, p.err));
+            if (ok && (pend & 1u))
+              ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * v_slot, v_par, abort_flag, p.err));
+            if (!ok) break;
+            if (pv_reads) {
+              tc_fence_after();
+              const uint64_t off = (uint64_t)((v_slot * C::kSlotBytes) >> 4);
+              const uint32_t first = pv_item == 0 ? 0u : 1u;
+              if (!gp) {
 #pragma unroll
-              for (int kk = 0; kk < kKeys / 16; ++kk)
-                mma_ts(d_o, d_s + kk * 8, dv_band + off + (uint64_t)(kk * 128), kIdescPV,
-                       kk > 0 ? 1u : first);
+                for (int kk = 0; kk < kKeys / 32; ++kk)
+                  mma_ts_warp(d_o, d_s + kk * 8, dv_band + off + (uint64_t)(kk * 128), kIdescPV,
+                              kk > 0 ? 1u : first);
+                ok = __all_sync(0xffffffffu, wait_bar(p_full, pv & 1u, abort_flag, p.err));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = kKeys / 32; kk < kKeys / 16; ++kk)
+                  mma_ts_warp(d_o, d_s + kk * 8, dv_band + off + (uint64_t)(kk * 128), kIdescPV, 1u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < kGKeys / 16; ++kk)
+                  mma_ts_warp(d_o, d_s + kk * 8, dv_glob + off + (uint64_t)(kk * 128), kIdescPV,
+                              kk > 0 ? 1u : first);
+              }
+              ++pv;
+              ++pv_item;
+              mma_commit_warp(B.slot_empty + 8 * v_slot);
+              if (ip == last) mma_commit_warp(B.o_final + 8 * u);
             } else {
-#pragma unroll
-              for (int kk = 0; kk < kGKeys / 16; ++kk)
-                mma_ts(d_o, d_s + kk * 8, dv_glob + off + (uint64_t)(kk * 128), kIdescPV,
-                       kk > 0 ? 1u : first);
+              mbar_arrive_warp(B.slot_empty + 8 * v_slot);
             }
-            ++pv;
-            mma_commit(B.slot_empty + 8 * v_slot);
-            if (ip == last) mma_commit(B.o_final + 8 * u);
-          } else {
-            mbar_arrive(B.slot_empty + 8 * v_slot);
           }
-        }
-        if (i < n_tiles) {
-          const bool gc = i >= w.nb;
-          const bool reads = gc || (i >= a_u && i < b_u);
-          ok = wait_bar(B.slot_full + 8 * k_slot, k_par, abort_flag, p.err);
-          // ping-pong handshake (position i of tile 1 follows position i of tile 0)
-          if (ok && w.active[1]) {
-            if (u == 1)
-              ok = wait_bar(B.s_issued, i & 1, abort_flag, p.err);
-            else if (i > 0)
-              ok = wait_bar(B.s_issued + 8, (i - 1) & 1, abort_flag, p.err);
-          }
-          if (!ok) break;
-          if (reads) {
-            tc_fence_after();
-            const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
-            if (!gc) {
+          if (do_s) {
+            if (pend & 2u)
+              ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * k_slot, k_par, abort_flag, p.err));
+            if (ok && (pend & 4u)) ok = __all_sync(0xffffffffu, wait_bar(hs_bar, hs_par, abort_flag, p.err));
+            if (!ok) break;
+            if (s_reads) {
+              tc_fence_after();
+              const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
+              if (!gc) {
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
-                       dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk)
+                  mma_ss_warp(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                              dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                  mma_ss_warp(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                              dk + (((kk >> 2) * (kGKeys * 128) + (kk & 3) * 32) >> 4), kIdescSg, kk > 0);
+              }
+              mma_commit_warp(s_full);
+              if (!kStagedStore && i == last) mma_commit_warp(B.q_empty + 8 * qb);  // Q buffer free
+              mma_commit_warp(B.slot_empty + 8 * k_slot);
             } else {
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
-                       dk + (((kk >> 2) * (kGKeys * 128) + (kk & 3) * 32) >> 4), kIdescSg, kk > 0);
+              mbar_arrive_warp(B.slot_empty + 8 * k_slot);
             }
-            mma_commit(s_full);
-            mma_commit(B.slot_empty + 8 * k_slot);
-          } else {
-            mbar_arrive(B.slot_empty + 8 * k_slot);
+            mbar_arrive_warp(B.s_issued + 8 * u);  // S_u(g) issued (or not needed)
+            ++g;
+            k_slot += 2;  // advance by two loads (K_i, V_i)
+            if (k_slot >= NS) {
+              k_slot -= NS;
+              k_par ^= 1;
+            }
           }
-          mbar_arrive(B.s_issued + 8 * u);  // S_u(i) issued (or not needed)
-        }
-        k_slot += 2;  // advance by two loads (K_i, V_i)
-        if (k_slot >= NS) {
-          k_slot -= NS;
-          k_par ^= 1;
         }
       }
       // everything this thread issued has completed before TMEM is released
-      mma_commit(B.mma_done + 8 * u);
+      mma_commit_warp(B.mma_done + 8 * u);
+      __syncwarp();
       wait_bar(B.mma_done + 8 * u, 0, abort_flag, nullptr, false);
     }
   } else if (warp < 8) {
@@ -711,70 +881,93 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     const uint32_t lane_addr = (uint32_t)((row >> 5) * 32) << 16;
     const uint32_t t_s = tmem + lane_addr + u * 128;
     const uint32_t t_o = tmem + lane_addr + 256 + u * 128;
-    const bool act_u = u ? w.active[1] : w.active[0];
-    const int nlo_u = u ? w.n_lo[1] : w.n_lo[0];
-    const int ncnt_u = u ? w.n_cnt[1] : w.n_cnt[0];
-    const int n = act_u ? ncnt_u + w.ng : 0;
     const float sl = p.scale_log2;
-    const int t_q = GLOBAL ? 0 : (w.q_tile + u) * kRows + row;  // class coordinate
     const int half = p.half;
     const int bar_id = 1 + u;
-    float m_run = -INFINITY, l_run = 0.f;
+    int32_t *g_list = g_lists + u * SA_MAX_GLOBALS;
+    uint32_t scnt = 0, ocnt = 0, jq = 0;  // jq: query tiles of earlier items
     bool ok = true;
-
-    for (int i = 0; i < n && ok; ++i) {
-      const int pos = seq_pos_s(w, nlo_u, ncnt_u, i);
-      const bool gt = pos >= w.nb;
-      ok = __all_sync(0xffffffffu, wait_bar(B.s_full + 8 * u, i & 1, abort_flag, p.err));
-      if (!ok) break;
-      tc_fence_after();
-      if (!gt) {
-        const int kb = GLOBAL ? (w.key0 + pos * kKeys) : (w.lo + pos) * kKeys;
-        bool full;
-        int c_lo = 0, c_hi = kKeys - 1;
-        if (GLOBAL) {
-          full = kb + kKeys <= w.key_end;
-          c_hi = w.key_end - 1 - kb;
-        } else {
-          const int q0 = (w.q_tile + u) * kRows;
-          full = (kb + kKeys - 1 - q0 <= half) && (q0 + kRows - 1 - kb <= half) &&
-                 (kb + kKeys <= w.len);
-          c_lo = t_q - half - kb;
-          c_hi = min(t_q + half, w.len - 1) - kb;
+    for (int item = item0; item < n_items && ok; item += stride) {
+      const Work w = make_work<GLOBAL>(P, item);
+      const bool act_u = u ? w.active[1] : w.active[0];
+      const uint32_t jt = jq + ((u == 1 && w.active[0]) ? 1u : 0u);  // this tile's load index
+      jq += (uint32_t)w.active[0] + (uint32_t)w.active[1];
+      if (!act_u) continue;
+      const uint32_t qb = jt % NQ;  // buffer holding Q_u; the output is staged there
+      const int nlo_u = u ? w.n_lo[1] : w.n_lo[0];
+      const int ncnt_u = u ? w.n_cnt[1] : w.n_cnt[0];
+      const int n = ncnt_u + w.ng;
+      const int t_q = GLOBAL ? 0 : (w.q_tile + u) * kRows + row;  // class coordinate
+      if (!GLOBAL && w.ng > 0) {
+        // global positions in this item's residue-class coordinates: g = r + d*t
+        // gives t; a global outside the class can never lie in a row's band.
+        // (The previous item's readers of this list passed the warpgroup's
+        // epilogue barrier before this point.)
+        for (int i = row; i < p.n_g; i += 128) {
+          const int gg = p.globals[i] - w.r;
+          g_list[i] = (gg >= 0 && gg % w.d == 0) ? gg / w.d : kFarAway;
         }
-        softmax_tile<kKeys, D>(t_s, t_o, sl, full ? kMaskNone : kMaskInterval, c_lo, c_hi,
-                               nullptr, 0, 0, 0, 0, 1, false, m_run, l_run);
-      } else {
-        const int g0 = (pos - w.nb) * kGKeys;
-        const bool dedup = (w.flags >> u) & 1;
-        softmax_tile<kGKeys, D>(t_s, t_o, sl, kMaskGlobal, 0, p.n_g - 1 - g0, g_list, g0, t_q,
-                                half, w.r, w.d, dedup, m_run, l_run);
+        named_bar_sync(bar_id, 128);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(B.p_full + 8 * u);
-    }
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int i = 0; i < n && ok; ++i) {
+        const int pos = seq_pos_s(w, nlo_u, ncnt_u, i);
+        const bool gt = is_global_pos(w, pos);
+        ok = __all_sync(0xffffffffu, wait_bar(B.s_full + 8 * u, scnt & 1u, abort_flag, p.err));
+        ++scnt;
+        if (!ok) break;
+        tc_fence_after();
+        if (!gt) {
+          const int kb = GLOBAL ? (w.key0 + band_index(w, pos) * kKeys) : (w.lo + band_index(w, pos)) * kKeys;
+          bool full;
+          int c_lo = 0, c_hi = kKeys - 1;
+          if (GLOBAL) {
+            full = kb + kKeys <= w.key_end;
+            c_hi = w.key_end - 1 - kb;
+          } else {
+            const int q0 = (w.q_tile + u) * kRows;
+            full = (kb + kKeys - 1 - q0 <= half) && (q0 + kRows - 1 - kb <= half) &&
+                   (kb + kKeys <= w.len);
+            c_lo = t_q - half - kb;
+            c_hi = min(t_q + half, w.len - 1) - kb;
+          }
+          softmax_tile<kKeys, D>(t_s, t_o, sl, full ? kMaskNone : kMaskInterval, c_lo, c_hi, nullptr,
+                                 0, 0, 0, false, B.p_half + 8 * u, lane, m_run, l_run);
+        } else {
+          const int g0 = global_index(w, pos) * kGKeys;
+          const bool dedup = (w.flags >> u) & 1;
+          softmax_tile<kGKeys, D>(t_s, t_o, sl, kMaskGlobal, 0, p.n_g - 1 - g0, g_list, g0, t_q,
+                                  half, dedup, B.p_half + 8 * u, lane, m_run, l_run);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (gt) mbar_arrive(B.p_half + 8 * u);  // a global tile is written in one piece
+          mbar_arrive(B.p_full + 8 * u);
+        }
+      }
 
-    if (n > 0) {
       // every thread of the warpgroup takes part in the same barriers, so the
       // decision to write the tile is made jointly
-      bool fin = ok && wait_bar(B.o_final + 8 * u, 0, abort_flag, p.err);
+      bool fin = ok && wait_bar(B.o_final + 8 * u, ocnt & 1u, abort_flag, p.err);
+      ++ocnt;
       fin = named_bar_and(bar_id, 128, fin);
-      if (fin) tc_fence_after();
-      if (!GLOBAL) {
-        // normalise, stage the bf16 tile in this query tile's (now idle) smem
-        // in the TMA 128-byte-swizzle layout, and store it with TMA
-        uint8_t *stage = smem + u * C::kQBytes;
-        if (fin) {
-          const float inv = rcp_approx(l_run);
+      ok = fin;
+      if (!fin) break;
+      tc_fence_after();
+      if (!GLOBAL && !kStagedStore) {
+        // normalise and write this thread's row straight from registers
+        const float inv = rcp_approx(l_run);
+        const bool valid = t_q < w.len;
+        const int64_t pos_q = (int64_t)w.r + (int64_t)w.d * t_q;
+        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                                ((int64_t)w.bh * p.N + pos_q) * D);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(t_o + c * 32, r);
-            const int h = (c * 32) / 64;
-            const int chunk0 = ((c * 32) % 64) / 8;  // first 16-byte chunk in the row
-            uint8_t *rowp = stage + h * (kRows * 128) + row * 128;
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_o + c * 32, r);  // collective: every lane loads
+          if (valid) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint4 v;
@@ -782,44 +975,75 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
               v.y = pack_bf16(__uint_as_float(r[q4 * 8 + 2]) * inv, __uint_as_float(r[q4 * 8 + 3]) * inv);
               v.z = pack_bf16(__uint_as_float(r[q4 * 8 + 4]) * inv, __uint_as_float(r[q4 * 8 + 5]) * inv);
               v.w = pack_bf16(__uint_as_float(r[q4 * 8 + 6]) * inv, __uint_as_float(r[q4 * 8 + 7]) * inv);
-              const int phys = (chunk0 + q4) ^ (row & 7);
-              *reinterpret_cast<uint4 *>(rowp + phys * 16) = v;
+              orow[c * 4 + q4] = v;
             }
           }
-          if (p.lse && t_q < w.len) {
-            const int64_t pos_q = (int64_t)w.r + (int64_t)w.d * t_q;
-            p.lse[(int64_t)w.bh * p.N + pos_q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
-          }
-          fence_proxy_async_smem();
         }
+        if (p.lse && valid)
+          p.lse[(int64_t)w.bh * p.N + pos_q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+      } else if (!GLOBAL) {
+        // normalise, stage the bf16 tile in this tile's query buffer (its last
+        // S MMA has completed) in the TMA 128-byte-swizzle layout, and store it
+        // with TMA; the buffer is handed back to the Q producer once the store
+        // has read it
+        uint8_t *stage = smem + qb * C::kQBytes;
+        const float inv = rcp_approx(l_run);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_o + c * 32, r);
+          const int h = (c * 32) / 64;
+          const int chunk0 = ((c * 32) % 64) / 8;  // first 16-byte chunk in the row
+          uint8_t *rowp = stage + h * (kRows * 128) + row * 128;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(r[q4 * 8 + 0]) * inv, __uint_as_float(r[q4 * 8 + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(r[q4 * 8 + 2]) * inv, __uint_as_float(r[q4 * 8 + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(r[q4 * 8 + 4]) * inv, __uint_as_float(r[q4 * 8 + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(r[q4 * 8 + 6]) * inv, __uint_as_float(r[q4 * 8 + 7]) * inv);
+            const int phys = (chunk0 + q4) ^ (row & 7);
+            *reinterpret_cast<uint4 *>(rowp + phys * 16) = v;
+          }
+        }
+        if (p.lse && t_q < w.len) {
+          const int64_t pos_q = (int64_t)w.r + (int64_t)w.d * t_q;
+          p.lse[(int64_t)w.bh * p.N + pos_q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+        }
+        fence_proxy_async_smem();
         named_bar_sync(bar_id, 128);
-        if (fin && row == 0) {
+        if (row == 0) {
           const int ls = w.slot - P.slot_base;
           for (int h = 0; h < C::kHalves; ++h)
             tma_store_3d(&P.maps.o[ls], smem_u32(stage) + h * (kRows * 128), 64 * h,
-                         (w.q_tile + u) * kRows, w.bh);
-          tma_store_commit_and_drain();
+                         (w.q_tile + u) * kRows, w.bh);  // rows past the class end are clipped
+          tma_store_commit_and_wait_read();
+          mbar_arrive(B.q_empty + 8 * qb);
         }
-      } else if (fin) {
-        const int g = u * kRows + row;
-        const int64_t slot = ((int64_t)w.bh * p.n_chunks + w.chunk) * p.g_pad + g;
+      } else {
+        const int gr = q_row_of<GLOBAL>(w, u) + row;
+        const int64_t slot = ((int64_t)w.bh * p.n_chunks + w.chunk) * p.g_pad + gr;
         float4 *dst = reinterpret_cast<float4 *>(p.part_o + slot * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(t_o + c * 32, r);  // collective: every lane loads
-          if (g < p.n_g) {
+          if (gr < p.n_g) {
 #pragma unroll
             for (int x = 0; x < 8; ++x)
               dst[c * 8 + x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
                                            __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
           }
         }
-        if (g < p.n_g) {
+        if (gr < p.n_g) {
           p.part_ml[slot * 2 + 0] = m_run;
           p.part_ml[slot * 2 + 1] = l_run;
         }
+        if (kStagedStore && row == 0) mbar_arrive(B.q_empty + 8 * qb);  // every S MMA has completed
       }
+      // O_u has been read out (tcgen05.ld waits): the next item's first PV_u,
+      // issued only after this warpgroup's next P arrival, may overwrite it
+      tc_fence_before();
     }
   }
 
@@ -863,13 +1087,21 @@ cudaError_t make_map(CUtensorMap *m, const void *base, int D, uint64_t rows, uin
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Persistent launch: one CTA per SM (at most one work item each), every CTA
+// striding over the launch's n_items work items.
 template <int D, bool GLOBAL>
-cudaError_t launch(Params &P, int grid, cudaStream_t s) {
-  if (grid <= 0) return cudaSuccess;
-  constexpr int smem = Cfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(tc_attention_kernel<D, GLOBAL>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t launch(Params &P, int n_items, cudaStream_t s) {
+  if (n_items <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  constexpr int smem = Cfg<D>::kSmemBytes;
+  e = cudaFuncSetAttribute(tc_attention_kernel<D, GLOBAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem);
+  if (e != cudaSuccess) return e;
+  P.n_items = n_items;
+  const int grid = std::min(n_items, std::max(sms, 1));
   tc_attention_kernel<D, GLOBAL><<<grid, kThreads, smem, s>>>(P);
   return cudaGetLastError();
 }
