@@ -30,9 +30,11 @@
 // also write the finished rows), warps 4-7 softmax of Q_1, warp 8 TMA producers
 // (lane 0 keys/values, lane 1 queries), warp 9 MMA issuer of Q_0 (and TMEM
 // allocator), warp 10 MMA issuer of Q_1.  TMEM: S_0 cols [0,128), S_1 [128,256), O_0
-// [256,256+D), O_1 [384,384+D).  Shared memory: two query-tile buffers (used
-// alternately, so the next item's Q_0 can land while Q_1 is still in use),
-// then a ring of key/value slots (one K or V tile each), then barriers.  All tiles use the
+// [256,256+D), O_1 [384,384+D).  Shared memory: three query-tile buffers
+// (used in rotation, so the next item's first query tile can land while both
+// current ones are in use; a finished output tile is staged in its query
+// tile's buffer), then a ring of key/value slots (one K or V tile each), then
+// barriers.  All tiles use the
 // 128-byte swizzle that TMA writes and the UMMA descriptors read.
 //
 // Every wait on an mbarrier is bounded: after kWaitLimitNs the waiting thread
@@ -93,7 +95,7 @@ struct Cfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kAux = 3072;  // barriers, flags, global positions (class coordinates)
   static constexpr int kSmemMax = 232448;
-  static constexpr int kQBufs = 2;   // query tiles alternate between two buffers
+  static constexpr int kQBufs = 3;   // query tiles rotate through three buffers
   static constexpr int kSlots0 = (kSmemMax - kQBufs * kQBytes - kAux) / kSlotBytes;
   static constexpr int kSlots = kSlots0 > 12 ? 12 : kSlots0;
   static constexpr int kSmemBytes = kQBufs * kQBytes + kSlots * kSlotBytes + kAux;
@@ -490,19 +492,28 @@ __device__ __forceinline__ void load_scores(uint32_t t_s, float neg_scale, int m
   }
   // band tiles (kKeys wide) take the interval mask, global tiles (kGKeys
   // wide) the global one
+  // branch-free: a compare and a select per column (the bounds differ per row)
   if (W == kKeys && mode == kMaskInterval) {
-#pragma unroll
-    for (int x = 0; x < W; ++x)
-      if (x < c_lo || x > c_hi) s[x] = -INFINITY;
-  } else if (W == kGKeys && mode == kMaskGlobal) {
+    const uint32_t span = (uint32_t)(c_hi - c_lo);
 #pragma unroll
     for (int x = 0; x < W; ++x) {
-      bool valid = x <= c_hi;
-      if (valid && dedup) {
-        const int diff = t_q - globals[g0 + x];  // class coordinates; kFarAway is never in band
-        valid = diff > half || -diff > half;
+      const bool keep = (uint32_t)(x - c_lo) <= span;  // c_lo <= x <= c_hi
+      s[x] = keep ? s[x] : -INFINITY;
+    }
+  } else if (W == kGKeys && mode == kMaskGlobal) {
+    if (dedup) {
+      const uint32_t band = 2u * (uint32_t)half;
+#pragma unroll
+      for (int x = 0; x < W; ++x) {
+        // |t_q - t_g| > half, i.e. t_q - t_g + half outside [0, 2 half]; kFarAway
+        // (a global outside the class) is never in band
+        const bool out_of_band = (uint32_t)(t_q - globals[g0 + x] + half) > band;
+        const bool keep = (x <= c_hi) & out_of_band;
+        s[x] = keep ? s[x] : -INFINITY;
       }
-      if (!valid) s[x] = -INFINITY;
+    } else {
+#pragma unroll
+      for (int x = 0; x < W; ++x) s[x] = x <= c_hi ? s[x] : -INFINITY;
     }
   }
 }
@@ -656,8 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
   if (warp == 8 && lane == 1) {
     // ------------------------------------------------------------- Q producer
     // Query tiles are loaded in order (item by item, tile 0 then tile 1) into
-    // the buffers 0, 1, 0, 1, ...; a buffer is refilled once the output tile
-    // staged in it has been stored.  The following item's query rows are
+    // the buffers 0, 1, 2, 0, ...; a buffer is refilled once the output tile
+    // staged in it has been stored, so the next item's first query tile lands
+    // in the spare buffer while the current item is still running.  The following item's query rows are
     // prefetched into L2.
     {
       uint32_t j = 0;  // query tiles loaded so far
