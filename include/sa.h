@@ -107,6 +107,39 @@ sa_status sa_count_pairs(int N, int window, const int32_t *dilation, int H,
                          const int32_t *global_idx, int n_global, int64_t *per_head,
                          int64_t *total);
 
+/*
+ * sa_forward_chunked -- GMAT chunked self-attention with a global memory
+ * ("GMAT: Global Memory Augmentation for Transformers", subsection "Chunked
+ * self-attention", with the memory of section "Global Memory").  The sequence
+ * of N positions is [memory; main]: positions [0, n_memory) are memory tokens,
+ * which score every position and are scored by every position; the main
+ * positions are cut into contiguous chunks of `chunk` positions starting at
+ * n_memory (the last chunk may be shorter), and a main position scores the
+ * main positions of its own chunk plus the memory.  With n_memory = 0 each
+ * chunk is plain attention over `chunk` positions; with chunk >= N - n_memory
+ * it is plain attention over the whole sequence.
+ *
+ *  q, k, v, out, lse, B, H, N, D, scale, dtype, stream: as sa_forward_lse
+ *    (device pointers, contiguous [B, H, N, D], 16-byte aligned; lse may be
+ *    NULL; output dtype = input dtype).
+ *  n_memory  0 <= n_memory <= N, at most SA_MAX_GLOBALS (else
+ *            SA_ERR_UNSUPPORTED).
+ *  chunk     >= 1.
+ *  Errors: SA_ERR_INVALID_ARG / SA_ERR_UNSUPPORTED before any launch, as for
+ *  sa_forward.  Asynchronous on `stream`.
+ */
+sa_status sa_forward_chunked(const void *q, const void *k, const void *v, void *out, float *lse,
+                             int B, int H, int N, int D, int n_memory, int chunk, float scale,
+                             sa_dtype dtype, sa_stream_t stream);
+
+/*
+ * sa_count_pairs_chunked -- exact number of in-mask (i, j) pairs of one head of
+ * sa_forward_chunked: n_memory * N for the memory rows plus, per chunk of
+ * length c, c * (n_memory + c).  Host only.  Same validation as
+ * sa_forward_chunked; per_head must be non-null.
+ */
+sa_status sa_count_pairs_chunked(int N, int n_memory, int chunk, int64_t *per_head);
+
 /* Thread-local description of the last non-OK status on this host thread. */
 const char *sa_last_error(void);
 

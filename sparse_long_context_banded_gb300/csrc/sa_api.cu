@@ -110,7 +110,7 @@ void free_schedule(DeviceSchedule &s) {
 std::string schedule_key(const Problem &p, int family) {
   std::string k;
   auto put = [&k](const void *x, size_t n) { k.append(static_cast<const char *>(x), n); };
-  int head[7] = {family, p.B, p.H, p.N, p.D, p.window, (int)p.globals.size()};
+  int head[9] = {family, p.B, p.H, p.N, p.D, p.window, (int)p.globals.size(), p.chunk, p.memory};
   put(head, sizeof head);
   put(p.dilation.data(), sizeof(int32_t) * p.dilation.size());
   put(p.globals.data(), sizeof(int32_t) * p.globals.size());
@@ -194,7 +194,7 @@ struct StageTimer {
 sa_status forward_impl(const void *q, const void *k, const void *v, void *out, float *lse,
                        int B, int H, int N, int D, int window, const int32_t *dilation,
                        const int32_t *global_idx, int n_global, float scale, sa_dtype dtype,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, int chunk = 0, int memory = 0) {
   if (!q || !k || !v || !out) return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be non-null");
   if (n_global < 0) return fail(SA_ERR_INVALID_ARG, "n_global must be >= 0");
   if (n_global > 0 && !global_idx)
@@ -220,6 +220,8 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
     p.dilation.assign(H, 1);
   p.scale = scale;
   p.dtype = dtype;
+  p.chunk = chunk;
+  p.memory = memory;
   for (int i = 0; i < n_global; ++i)
     if (global_idx[i] < 0 || global_idx[i] >= N)
       return fail(SA_ERR_INVALID_ARG, "global_idx[%d] = %d outside [0, %d)", i, global_idx[i], N);
@@ -256,7 +258,9 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   dp.N = N;
   dp.D = D;
   dp.H = H;
-  dp.half = p.half;
+  dp.half = std::min(p.half, p.N);  // a wider band changes nothing
+  dp.chunk = p.chunk;
+  dp.memory = p.memory;
   dp.scale_log2 = scale * 1.4426950408889634f;
   dp.globals = sched->globals;
   dp.n_g = (int)p.globals.size();
@@ -353,6 +357,31 @@ extern "C" sa_status sa_forward_lse(const void *q, const void *k, const void *v,
                                     sa_stream_t stream) {
   return forward_impl(q, k, v, out, lse, B, H, N, D, window, dilation, global_idx, n_global,
                       scale, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" sa_status sa_forward_chunked(const void *q, const void *k, const void *v, void *out,
+                                        float *lse, int B, int H, int N, int D, int n_memory,
+                                        int chunk, float scale, sa_dtype dtype,
+                                        sa_stream_t stream) {
+  if (chunk < 1) return fail(SA_ERR_INVALID_ARG, "chunk must be >= 1 (got %d)", chunk);
+  if (n_memory < 0 || n_memory > N)
+    return fail(SA_ERR_INVALID_ARG, "n_memory = %d outside [0, N = %d]", n_memory, N);
+  if (n_memory > SA_MAX_GLOBALS)
+    return fail(SA_ERR_UNSUPPORTED, "%d memory tokens (at most %d)", n_memory, SA_MAX_GLOBALS);
+  std::vector<int32_t> mem(n_memory);
+  for (int i = 0; i < n_memory; ++i) mem[i] = i;
+  return forward_impl(q, k, v, out, lse, B, H, N, D, 0, nullptr, mem.data(), n_memory, scale,
+                      dtype, reinterpret_cast<cudaStream_t>(stream), chunk, n_memory);
+}
+
+extern "C" sa_status sa_count_pairs_chunked(int N, int n_memory, int chunk, int64_t *per_head) {
+  if (N < 1) return fail(SA_ERR_INVALID_ARG, "N must be >= 1 (got %d)", N);
+  if (chunk < 1) return fail(SA_ERR_INVALID_ARG, "chunk must be >= 1 (got %d)", chunk);
+  if (n_memory < 0 || n_memory > N)
+    return fail(SA_ERR_INVALID_ARG, "n_memory = %d outside [0, N = %d]", n_memory, N);
+  if (!per_head) return fail(SA_ERR_INVALID_ARG, "per_head must be non-null");
+  *per_head = pairs_chunked(N, n_memory, chunk);
+  return SA_OK;
 }
 
 extern "C" sa_status sa_count_pairs(int N, int window, const int32_t *dilation, int H,

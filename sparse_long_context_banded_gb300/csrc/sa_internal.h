@@ -43,15 +43,40 @@ struct GlobalItem {
   int32_t pad;
 };
 
-// Host-side description of one call.
+// Host-side description of one call.  Two mask patterns share every kernel:
+//   band (chunk == 0): row i scores |i-j| <= half*d, d | (i-j), plus the globals;
+//   chunked (chunk > 0): positions [0, memory) are the globals (GMAT memory),
+//   and a main position i >= memory scores the main positions of its chunk,
+//   (i-memory)/chunk, plus the memory.
 struct Problem {
   int B, H, N, D;
   int window, half;
-  std::vector<int32_t> dilation;  // per head
+  std::vector<int32_t> dilation;  // per head (all 1 for the chunked pattern)
   std::vector<int32_t> globals;   // sorted, unique
   float scale;
   sa_dtype dtype;
+  int chunk = 0;   // chunk length C of the chunked pattern, 0 for the band pattern
+  int memory = 0;  // memory tokens M of the chunked pattern
 };
+
+// Non-global keys of row t (class coordinate; len positions in the class), as
+// the interval [lo, hi]: the band t-half..t+half, or the row's chunk.  Rows
+// inside the memory (global rows, recomputed densely) take chunk 0.  Both lo
+// and hi never decrease with t, so a tile of rows reads keys lo(first row) ..
+// hi(last row).
+#if defined(__CUDACC__)
+__host__ __device__
+#endif
+inline void row_keys(int half, int chunk, int memory, int len, int t, int &lo, int &hi) {
+  if (chunk > 0) {
+    const int c = t >= memory ? (t - memory) / chunk : 0;
+    lo = memory + c * chunk;
+    hi = (lo + chunk < len ? lo + chunk : len) - 1;
+  } else {
+    lo = t - half;
+    hi = (t + half < len - 1 ? t + half : len - 1);
+  }
+}
 
 // Tiling of one kernel family.
 struct Tiling {
@@ -80,6 +105,7 @@ std::string validate(const Problem &p);
 std::vector<int32_t> global_set(const int32_t *idx, int n);
 Schedule build_schedule(const Problem &p, const Tiling &t);
 int64_t pairs_of_head(int N, int half, int d, const std::vector<int32_t> &globals);
+int64_t pairs_chunked(int N, int memory, int chunk);
 
 // Sets the thread-local message that sa_last_error() returns; returns s.
 sa_status record_error(sa_status s, const char *message);

@@ -21,6 +21,7 @@ struct DevProblem {
   float *lse;       // [B*H*N] or null
   int N, D, H;
   int half;         // floor(window / 2)
+  int chunk, memory;  // chunked pattern (chunk > 0): chunk length, memory tokens
   float scale_log2; // scale * log2(e): scores are kept in base-2 units
   const int32_t *globals;  // device, sorted unique, n_g entries
   int n_g, g_pad;

@@ -38,6 +38,15 @@ std::string validate(const Problem &p) {
       return buf;
     }
   if (!std::isfinite(p.scale)) return "scale must be finite";
+  if (p.chunk < 0) return "chunk must be >= 0";
+  if (p.chunk > 0) {
+    if (p.memory < 0 || p.memory > p.N) {
+      snprintf(buf, sizeof buf, "memory tokens %d outside [0, %d]", p.memory, p.N);
+      return buf;
+    }
+    for (int h = 0; h < p.H; ++h)
+      if (p.dilation[h] != 1) return "the chunked pattern takes no dilation";
+  }
   if (p.dtype != SA_BF16 && p.dtype != SA_FP32) return "unknown dtype";
   const double elems = (double)p.B * p.H * p.N * std::max(p.D, 1);
   if (elems > 9.0e18) return "tensor too large";
@@ -85,9 +94,20 @@ int64_t pairs_of_head(int N, int half, int d, const std::vector<int32_t> &G) {
   return (band_all - band_g) + rows_ng * n_g - g_in_band_rows + n_g * (int64_t)N;
 }
 
+// GMAT chunked pattern: M dense memory rows; a main row scores the M memory
+// keys and the main keys of its chunk.
+int64_t pairs_chunked(int N, int memory, int chunk) {
+  int64_t n = (int64_t)memory * N;
+  for (int64_t start = memory; start < N; start += chunk) {
+    const int64_t len = std::min<int64_t>(chunk, N - start);
+    n += len * (memory + len);
+  }
+  return n;
+}
+
 Schedule build_schedule(const Problem &p, const Tiling &t) {
   Schedule s;
-  const int64_t half = p.half;
+  const int half = std::min(p.half, p.N);  // a wider band changes nothing
   // residue-class slots, one group per distinct dilation value
   std::vector<int32_t> dvals(p.dilation);
   std::sort(dvals.begin(), dvals.end());
@@ -131,8 +151,16 @@ Schedule build_schedule(const Problem &p, const Tiling &t) {
             }
             const int64_t row_lo = tt * t.rows;
             const int64_t row_hi = std::min(len - 1, row_lo + t.rows - 1);
-            const int64_t key_lo = std::max<int64_t>(0, row_lo - half);
-            const int64_t key_hi = std::min<int64_t>(len - 1, row_hi + half);
+            int reach_lo, reach_hi, unused;
+            row_keys(half, p.chunk, p.memory, (int)len, (int)row_lo, reach_lo, unused);
+            row_keys(half, p.chunk, p.memory, (int)len, (int)row_hi, unused, reach_hi);
+            const int64_t key_lo = std::max<int64_t>(0, reach_lo);
+            const int64_t key_hi = std::min<int64_t>(len - 1, reach_hi);
+            if (key_hi < key_lo) {  // no non-global key for these rows (all memory)
+              it.k_lo[u] = 0;
+              it.k_hi[u] = -1;
+              continue;
+            }
             it.k_lo[u] = (int32_t)(key_lo / t.key_tile);
             it.k_hi[u] = (int32_t)(key_hi / t.key_tile);
             work += it.k_hi[u] - it.k_lo[u] + 1;
@@ -141,13 +169,14 @@ Schedule build_schedule(const Problem &p, const Tiling &t) {
             for (int32_t g : p.globals) {
               if ((g - r) % d != 0) continue;
               const int64_t tg = (g - r) / d;
-              if (tg >= row_lo - half && tg <= row_hi + half) {
+              if (tg >= reach_lo && tg <= reach_hi) {
                 it.flags |= 1 << u;
                 break;
               }
             }
           }
-          items.push_back({work, it});
+          if (it.k_hi[0] >= it.k_lo[0] || it.k_hi[1] >= it.k_lo[1])  // not all memory rows
+            items.push_back({work, it});
         }
       }
     }

@@ -158,6 +158,8 @@ __global__ void __launch_bounds__(NT) band_simt_kernel(DevProblem p) {
   const bool row_ok = t_row < sl.len;
   const int64_t pos_row = sl.r + (int64_t)sl.d * t_row;
   const int half = p.half;
+  int key_lo, key_hi;  // the row's non-global keys (band or chunk), class coordinates
+  row_keys(half, p.chunk, p.memory, sl.len, t_row, key_lo, key_hi);
 
   for (int g = tid; g < p.n_g; g += NT) Gs[g] = p.globals[g];
   load_rows<T, D>(Qs, p.q, cls_base + (int64_t)it.q_tile * QT * cls_stride, cls_stride,
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(NT) band_simt_kernel(DevProblem p) {
     simt_tile<D>(Qs, Ks, Vs, Ps, row, qd, p.scale_log2,
                  [&](int c) {
                    const int tk = t0 + c;
-                   return row_ok && tk < sl.len && abs(tk - t_row) <= half;
+                   return row_ok && tk < sl.len && tk >= key_lo && tk <= key_hi;
                  },
                  st_);
   }
@@ -192,7 +194,9 @@ __global__ void __launch_bounds__(NT) band_simt_kernel(DevProblem p) {
                  [&](int c) {
                    const int gi = g0 + c;
                    if (!row_ok || gi >= p.n_g) return false;
-                   // a global key already inside this row's band is not counted twice
+                   // a global key already among this row's band keys is not counted
+                   // twice (the chunked pattern's memory never is)
+                   if (p.chunk > 0) return true;
                    const int64_t diff = pos_row - Gs[gi];
                    const int64_t reach = (int64_t)half * sl.d;
                    const bool in_band = diff <= reach && -diff <= reach && diff % sl.d == 0;

@@ -390,14 +390,17 @@ __device__ __forceinline__ Work make_work(const Params &P, int item) {
     w.len = sl.len;
     w.q_tile = it.q_tile;
     w.flags = it.flags;
-    w.lo = it.k_lo[0];
-    int hi = it.k_hi[0];
+    int lo = 0x7fffffff, hi = -1;
     for (int u = 0; u < 2; ++u) {
       w.active[u] = it.k_hi[u] >= it.k_lo[u];
       w.n_lo[u] = it.k_lo[u];
       w.n_cnt[u] = w.active[u] ? it.k_hi[u] - it.k_lo[u] + 1 : 0;
-      if (w.active[u]) hi = max(hi, it.k_hi[u]);
+      if (w.active[u]) {
+        lo = min(lo, it.k_lo[u]);
+        hi = max(hi, it.k_hi[u]);
+      }
     }
+    w.lo = hi >= 0 ? lo : 0;
     w.nb = hi - w.lo + 1;
     w.ng = (p.n_g + kGKeys - 1) / kGKeys;
   } else {
@@ -937,11 +940,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
             full = kb + kKeys <= w.key_end;
             c_hi = w.key_end - 1 - kb;
           } else {
+            // the tile is full when every row's key interval covers it; the
+            // intervals only move forward with the row, so the first row has
+            // the earliest end and the last row the latest start
             const int q0 = (w.q_tile + u) * kRows;
-            full = (kb + kKeys - 1 - q0 <= half) && (q0 + kRows - 1 - kb <= half) &&
-                   (kb + kKeys <= w.len);
-            c_lo = t_q - half - kb;
-            c_hi = min(t_q + half, w.len - 1) - kb;
+            int lo_last, hi_first, r_lo, r_hi, unused;
+            row_keys(half, p.chunk, p.memory, w.len, q0 + kRows - 1, lo_last, unused);
+            row_keys(half, p.chunk, p.memory, w.len, q0, unused, hi_first);
+            full = lo_last <= kb && hi_first >= kb + kKeys - 1;
+            row_keys(half, p.chunk, p.memory, w.len, t_q, r_lo, r_hi);
+            c_lo = r_lo - kb;
+            c_hi = r_hi - kb;
           }
           softmax_tile<kKeys, D>(t_s, t_o, sl, full ? kMaskNone : kMaskInterval, c_lo, c_hi, nullptr,
                                  0, 0, 0, false, B.p_half + 8 * u, lane, m_run, l_run);

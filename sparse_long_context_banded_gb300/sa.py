@@ -44,6 +44,8 @@ SIGNATURES = {
     "sa_version": (ctypes.c_char_p, []),
     "sa_forward_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I32P, _I32P, _I,
                                 _F, _I, _VP]),
+    "sa_forward_chunked": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _VP]),
+    "sa_count_pairs_chunked": (_I, [_I, _I, _I, _I64P]),
 }
 SA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -145,6 +147,41 @@ def forward(q, k, v, window: int, dilation: Sequence[int] | None = None,
             st = load().sa_forward_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                        lse.data_ptr(), B, H, N, D, int(window), _ptr(dil),
                                        _ptr(g), int(g.size), sc, dt, h_stream)
+    _check(st)
+    return out
+
+
+def count_pairs_chunked(N: int, n_memory: int, chunk: int) -> int:
+    """Exact in-mask pair count of one head of the chunked pattern (host only)."""
+    per = ctypes.c_int64(0)
+    _check(load().sa_count_pairs_chunked(int(N), int(n_memory), int(chunk), ctypes.byref(per)))
+    return int(per.value)
+
+
+def forward_chunked(q, k, v, n_memory: int, chunk: int, scale: Optional[float] = None,
+                    out=None, lse=None, stream=None):
+    """GMAT chunked attention with ``n_memory`` memory tokens at the front of the
+    sequence and ``chunk``-long chunks after them (sa_forward_chunked); torch
+    CUDA tensors [B, H, N, D], bfloat16 or float32.  Returns ``out``."""
+    import torch
+
+    dt = SA_BF16 if q.dtype == torch.bfloat16 else SA_FP32 if q.dtype == torch.float32 else None
+    if dt is None:
+        raise TypeError(f"unsupported dtype {q.dtype} (bfloat16 or float32)")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or t.shape != q.shape:
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one shape and dtype")
+    B, H, N, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sc = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    with torch.cuda.device(q.device):
+        st = load().sa_forward_chunked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                       None if lse is None else lse.data_ptr(), B, H, N, D,
+                                       int(n_memory), int(chunk), sc, dt,
+                                       ctypes.c_void_p(stream.cuda_stream))
     _check(st)
     return out
 
