@@ -90,6 +90,9 @@ class Oracle:
             ctypes.c_int, i32p, i32p, ctypes.c_int] + tail
         lib.oracle_forward_longformer.restype = ctypes.c_int
         lib.oracle_forward_gmat.argtypes = common + [ctypes.c_int] * 4 + tail
+        lib.oracle_forward_longformer_global_proj.argtypes = [
+            ctypes.c_void_p] * 6 + [ctypes.c_int] * 6 + [i32p, i32p, ctypes.c_int] + tail
+        lib.oracle_forward_longformer_global_proj.restype = ctypes.c_int
         lib.oracle_forward_gmat.restype = ctypes.c_int
         self.lib = lib
 
@@ -140,13 +143,14 @@ class Oracle:
 
     # -- forward -------------------------------------------------------------
     @staticmethod
-    def _inputs(q, k, v):
-        arrs = [np.ascontiguousarray(a) for a in (q, k, v)]
+    def _inputs(*tensors):
+        arrs = [np.ascontiguousarray(a) for a in tensors]
         dt = arrs[0].dtype
         if any(a.dtype != dt for a in arrs) or dt not in _DTYPE_CODE:
-            raise TypeError("q, k, v must share one dtype: uint16 (bf16 bits), float32 or float64")
+            raise TypeError("q, k, v (and global projections) must share one dtype: "
+                            "uint16 (bf16 bits), float32 or float64")
         if arrs[0].ndim != 4 or any(a.shape != arrs[0].shape for a in arrs):
-            raise ValueError("q, k, v must be [B, H, N, D] of one shape")
+            raise ValueError("q, k, v (and global projections) must be [B, H, N, D] of one shape")
         return arrs, _DTYPE_CODE[dt]
 
     @staticmethod
@@ -160,14 +164,20 @@ class Oracle:
 
     def forward_longformer(self, q, k, v, window: int, dilation=None, globals_=(),
                            scale: float | None = None, rows=None, threads: int | None = None,
-                           want_lse: bool = True):
+                           want_lse: bool = True, global_proj=None):
         """Masked-softmax attention in fp64.
 
         q, k, v: [B, H, N, D].  dilation: per-head list (None = all 1).
         rows: optional flattened row ids ((b*H + h)*N + i); None = every row.
+        global_proj: optional (qg, kg, vg) of q's shape and dtype -- separate
+        global projections: a global row then scores qg . kg over every key and
+        averages vg; the other rows use q, k, v throughout.
         Returns (out [B,H,N,D] or [n_rows,D], lse [B,H,N] or [n_rows]) as float64.
         """
-        (q, k, v), code = self._inputs(q, k, v)
+        if global_proj is not None:
+            (q, k, v, qg, kg, vg), code = self._inputs(q, k, v, *global_proj)
+        else:
+            (q, k, v), code = self._inputs(q, k, v)
         B, H, N, D = q.shape
         dil = np.ones(H, dtype=np.int32) if dilation is None else \
             np.ascontiguousarray(np.asarray(dilation, dtype=np.int32).reshape(-1))
@@ -178,10 +188,16 @@ class Oracle:
         r, n = self._rows(rows, B * H * N)
         out = np.empty((n, D), dtype=np.float64)
         lse = np.empty(n, dtype=np.float64) if want_lse else None
-        rc = self.lib.oracle_forward_longformer(
-            _ptr(q), _ptr(k), _ptr(v), code, B, H, N, D, int(window), _ptr(dil), _ptr(g),
-            int(g.size), sc, _ptr(r), int(n), _ptr(out), _ptr(lse),
-            int(threads or default_threads()))
+        if global_proj is not None:
+            rc = self.lib.oracle_forward_longformer_global_proj(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(qg), _ptr(kg), _ptr(vg), code, B, H, N, D,
+                int(window), _ptr(dil), _ptr(g), int(g.size), sc, _ptr(r), int(n), _ptr(out),
+                _ptr(lse), int(threads or default_threads()))
+        else:
+            rc = self.lib.oracle_forward_longformer(
+                _ptr(q), _ptr(k), _ptr(v), code, B, H, N, D, int(window), _ptr(dil), _ptr(g),
+                int(g.size), sc, _ptr(r), int(n), _ptr(out), _ptr(lse),
+                int(threads or default_threads()))
         if rc:
             raise MemoryError("oracle forward failed")
         if rows is None:

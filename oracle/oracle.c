@@ -300,6 +300,9 @@ void oracle_mask_gmat(int pattern, int N, int M, int window, int C,
 typedef struct {
   const mask_spec *ms;
   const void *q, *k, *v;
+  /* separate global projections (Longformer pattern), or NULL: a global row
+   * then scores q_g . k_g over all keys and averages v_g */
+  const void *qg, *kg, *vg;
   int dtype;
   int B, H, N, D;
   double scale;
@@ -310,6 +313,14 @@ typedef struct {
   int64_t begin, end;
   int status;
 } fwd_job;
+
+/* Is position i one of the Longformer pattern's global positions? */
+static int is_global(const mask_spec *ms, int i) {
+  int g;
+  for (g = 0; g < ms->n_globals; ++g)
+    if (ms->globals[g] == i) return 1;
+  return 0;
+}
 
 static void *fwd_worker(void *arg) {
   fwd_job *job = (fwd_job *)arg;
@@ -337,16 +348,22 @@ static void *fwd_worker(void *arg) {
     double *o = job->out + r * (int64_t)D;
     int j, d;
 
+    const void *qs = job->q, *ks = job->k, *vs = job->v;
+    if (job->qg && is_global(ms, i)) {
+      qs = job->qg;
+      ks = job->kg;
+      vs = job->vg;
+    }
     build_row(ms, head, i, row);
     for (d = 0; d < D; ++d)
-      qi[d] = load_elem(job->q, job->dtype, base + (int64_t)i * D + d);
+      qi[d] = load_elem(qs, job->dtype, base + (int64_t)i * D + d);
 
     /* scores over the masked set, and their maximum */
     for (j = 0; j < N; ++j) {
       double acc = 0.0;
       if (!row[j]) continue;
       for (d = 0; d < D; ++d)
-        acc += qi[d] * load_elem(job->k, job->dtype, base + (int64_t)j * D + d);
+        acc += qi[d] * load_elem(ks, job->dtype, base + (int64_t)j * D + d);
       s[j] = job->scale * acc;
       if (s[j] > m) m = s[j];
     }
@@ -358,7 +375,7 @@ static void *fwd_worker(void *arg) {
       e = exp(s[j] - m);
       z += e;
       for (d = 0; d < D; ++d)
-        o[d] += e * load_elem(job->v, job->dtype, base + (int64_t)j * D + d);
+        o[d] += e * load_elem(vs, job->dtype, base + (int64_t)j * D + d);
     }
     for (d = 0; d < D; ++d) o[d] /= z;
     if (job->lse) job->lse[r] = m + log(z);
@@ -370,7 +387,8 @@ static void *fwd_worker(void *arg) {
 }
 
 static int run_forward(const mask_spec *ms, const void *q, const void *k,
-                       const void *v, int dtype, int B, int H, int N, int D,
+                       const void *v, const void *qg, const void *kg, const void *vg,
+                       int dtype, int B, int H, int N, int D,
                        double scale, const int64_t *rows, int64_t n_rows,
                        double *out, double *lse, int threads) {
   fwd_job *jobs;
@@ -393,6 +411,9 @@ static int run_forward(const mask_spec *ms, const void *q, const void *k,
     job->q = q;
     job->k = k;
     job->v = v;
+    job->qg = qg;
+    job->kg = kg;
+    job->vg = vg;
     job->dtype = dtype;
     job->B = B;
     job->H = H;
@@ -434,8 +455,33 @@ int oracle_forward_longformer(const void *q, const void *k, const void *v,
   ms.dilation = dilation;
   ms.globals = globals;
   ms.n_globals = n_globals;
-  return run_forward(&ms, q, k, v, dtype, B, H, N, D, scale, rows, n_rows, out,
-                     lse, threads);
+  return run_forward(&ms, q, k, v, NULL, NULL, NULL, dtype, B, H, N, D, scale, rows,
+                     n_rows, out, lse, threads);
+}
+
+/* Longformer pattern with separate global projections (Ultralytics glossary
+ * "Longformer", section "How the Longformer attention works": global attention
+ * uses its own query, key and value projections).  Reading taken: a global row
+ * scores qg_i . kg_j over every key j and averages vg; every other row -- its
+ * band keys and its global keys alike -- uses q, k, v, as in sa_forward.
+ * qg, kg, vg: [B, H, N, D] like q, k, v (only the global rows of qg are read). */
+int oracle_forward_longformer_global_proj(const void *q, const void *k, const void *v,
+                                          const void *qg, const void *kg, const void *vg,
+                                          int dtype, int B, int H, int N, int D, int window,
+                                          const int32_t *dilation, const int32_t *globals,
+                                          int n_globals, double scale, const int64_t *rows,
+                                          int64_t n_rows, double *out, double *lse,
+                                          int threads) {
+  mask_spec ms;
+  memset(&ms, 0, sizeof ms);
+  ms.pattern = ORACLE_PATTERN_LONGFORMER;
+  ms.N = N;
+  ms.window = window;
+  ms.dilation = dilation;
+  ms.globals = globals;
+  ms.n_globals = n_globals;
+  return run_forward(&ms, q, k, v, qg, kg, vg, dtype, B, H, N, D, scale, rows, n_rows,
+                     out, lse, threads);
 }
 
 /* GMAT patterns over the concatenated [memory; main] sequence of length N. */
@@ -450,6 +496,6 @@ int oracle_forward_gmat(const void *q, const void *k, const void *v, int dtype,
   ms.M = M;
   ms.window = window;
   ms.C = C;
-  return run_forward(&ms, q, k, v, dtype, B, H, N, D, scale, rows, n_rows, out,
-                     lse, threads);
+  return run_forward(&ms, q, k, v, NULL, NULL, NULL, dtype, B, H, N, D, scale, rows,
+                     n_rows, out, lse, threads);
 }

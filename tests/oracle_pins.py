@@ -183,6 +183,27 @@ def pin_global_rows_dense(o):
         assert np.allclose(out[:, h:h + 1], ref_h, rtol=1e-11, atol=1e-12)
 
 
+def pin_global_projections(o):
+    """Separate global projections (Longformer glossary, "How the Longformer
+    attention works"): with qg, kg, vg = q, k, v the call is the plain pattern;
+    the non-global rows never read the global projections; each global row is
+    dense softmax attention of its qg row over kg, vg (a library routine)."""
+    N, D = 70, 16
+    G = [0, 33, 69]
+    q, k, v, qg, kg, vg = (randn((1, 2, N, D), 60 + s) for s in range(6))
+    plain, plain_lse = o.forward_longformer(q, k, v, 10, [1, 3], G)
+    same, same_lse = o.forward_longformer(q, k, v, 10, [1, 3], G, global_proj=(q, k, v))
+    assert np.array_equal(plain, same) and np.array_equal(plain_lse, same_lse)
+    out, _ = o.forward_longformer(q, k, v, 10, [1, 3], G, global_proj=(qg, kg, vg))
+    rest = [i for i in range(N) if i not in G]
+    assert np.array_equal(out[:, :, rest], plain[:, :, rest])
+    ref = sdpa(qg, kg, vg, None, 1 / math.sqrt(D))
+    for g in G:
+        assert np.allclose(out[:, :, g], ref[:, :, g], rtol=1e-11, atol=1e-12)
+        # and not the plain projections' answer
+        assert not np.allclose(out[:, :, g], plain[:, :, g], rtol=1e-3, atol=1e-3)
+
+
 def pin_gmat_band_is_longformer_with_memory_globals(o):
     """GMAT (memory prefix dense both ways + band on main tokens) has the same
     mask as the Longformer form over all M+L positions with globals {0..M-1}."""
@@ -285,5 +306,5 @@ ALL_PINS = [
     pin_brute_force_attention, pin_dense_limit, pin_global_rows_dense,
     pin_gmat_band_is_longformer_with_memory_globals, pin_memory_permutation,
     pin_shift_invariance, pin_dilation_is_band_per_residue, pin_chunked,
-    pin_bf16_decode,
+    pin_bf16_decode, pin_global_projections,
 ]

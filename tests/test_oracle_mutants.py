@@ -21,11 +21,12 @@ MUTANTS = {
     "global_row_not_dense": ("if (globals[g] == i) row_is_global = 1;", ""),
     "scale_dropped": ("s[j] = job->scale * acc;", "s[j] = acc;"),
     "key_index_transposed": (
-        "acc += qi[d] * load_elem(job->k, job->dtype, base + (int64_t)j * D + d);",
-        "acc += qi[d] * load_elem(job->k, job->dtype, base + (int64_t)i * D + d);"),
+        "acc += qi[d] * load_elem(ks, job->dtype, base + (int64_t)j * D + d);",
+        "acc += qi[d] * load_elem(ks, job->dtype, base + (int64_t)i * D + d);"),
     "value_from_keys": (
-        "o[d] += e * load_elem(job->v, job->dtype, base + (int64_t)j * D + d);",
-        "o[d] += e * load_elem(job->k, job->dtype, base + (int64_t)j * D + d);"),
+        "o[d] += e * load_elem(vs, job->dtype, base + (int64_t)j * D + d);",
+        "o[d] += e * load_elem(ks, job->dtype, base + (int64_t)j * D + d);"),
+    "global_rows_plain_keys": ("      ks = job->kg;", "      ks = job->k;"),
     "no_normalise": ("for (d = 0; d < D; ++d) o[d] /= z;", ""),
     "lse_without_max": ("job->lse[r] = m + log(z);", "job->lse[r] = log(z);"),
     "gmat_memory_column_dropped": ("if (row_mem || col_mem)", "if (row_mem)"),
