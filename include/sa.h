@@ -97,6 +97,28 @@ sa_status sa_forward_lse(const void *q, const void *k, const void *v, void *out,
                          sa_stream_t stream);
 
 /*
+ * sa_forward_global_proj -- sa_forward_lse with separate projections for the
+ * global attention (Ultralytics glossary "Longformer", section "How the
+ * Longformer attention works": the global attention has query, key and value
+ * projections of its own).  A global row i scores scale * <q_global_i,
+ * k_global_j> over every key j and averages v_global; every other row uses
+ * q, k, v for its band keys and its global keys alike, exactly as
+ * sa_forward_lse.  The mask, and so sa_count_pairs, is that of sa_forward.
+ *
+ *  q_global, k_global, v_global  device, [B,H,N,D] in `dtype`, 16-byte
+ *            aligned, non-null; read only.  Only the global rows of q_global
+ *            are read; k_global and v_global are read in full when
+ *            n_global > 0 and not at all otherwise.
+ *  Other arguments, errors and stream semantics: as sa_forward_lse.
+ */
+sa_status sa_forward_global_proj(const void *q, const void *k, const void *v,
+                                 const void *q_global, const void *k_global,
+                                 const void *v_global, void *out, float *lse, int B, int H,
+                                 int N, int D, int window, const int32_t *dilation,
+                                 const int32_t *global_idx, int n_global, float scale,
+                                 sa_dtype dtype, sa_stream_t stream);
+
+/*
  * sa_count_pairs -- exact number of (i, j) pairs in the mask, |S_i| summed
  * over i, per head (per_head[H], may be NULL) and over all heads of one batch
  * element (*total, may be NULL).  Host only, integer arithmetic, no GPU use.

@@ -194,16 +194,22 @@ struct StageTimer {
 sa_status forward_impl(const void *q, const void *k, const void *v, void *out, float *lse,
                        int B, int H, int N, int D, int window, const int32_t *dilation,
                        const int32_t *global_idx, int n_global, float scale, sa_dtype dtype,
-                       cudaStream_t stream, int chunk = 0, int memory = 0) {
+                       cudaStream_t stream, int chunk = 0, int memory = 0,
+                       const void *q_glob = nullptr, const void *k_glob = nullptr,
+                       const void *v_glob = nullptr) {
   if (!q || !k || !v || !out) return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be non-null");
+  if (!q_glob) q_glob = q;
+  if (!k_glob) k_glob = k;
+  if (!v_glob) v_glob = v;
   if (n_global < 0) return fail(SA_ERR_INVALID_ARG, "n_global must be >= 0");
   if (n_global > 0 && !global_idx)
     return fail(SA_ERR_INVALID_ARG, "global_idx is null but n_global = %d", n_global);
   if (H < 1) return fail(SA_ERR_INVALID_ARG, "H must be >= 1 (got %d)", H);
-  const void *ptrs[4] = {q, k, v, out};
-  for (int i = 0; i < 4; ++i)
+  const void *ptrs[7] = {q, k, v, out, q_glob, k_glob, v_glob};
+  for (int i = 0; i < 7; ++i)
     if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0)
-      return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+      return fail(SA_ERR_INVALID_ARG, "q, k, v, out (and the global projections) must be "
+                  "16-byte aligned");
   if (reinterpret_cast<uintptr_t>(lse) % 4 != 0)
     return fail(SA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
 
@@ -253,6 +259,9 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   dp.q = q;
   dp.k = k;
   dp.v = v;
+  dp.gq_src = q_glob;
+  dp.gk_src = k_glob;
+  dp.gv_src = v_glob;
   dp.out = out;
   dp.lse = lse;
   dp.N = N;
@@ -372,6 +381,20 @@ extern "C" sa_status sa_forward_chunked(const void *q, const void *k, const void
   for (int i = 0; i < n_memory; ++i) mem[i] = i;
   return forward_impl(q, k, v, out, lse, B, H, N, D, 0, nullptr, mem.data(), n_memory, scale,
                       dtype, reinterpret_cast<cudaStream_t>(stream), chunk, n_memory);
+}
+
+extern "C" sa_status sa_forward_global_proj(const void *q, const void *k, const void *v,
+                                            const void *q_global, const void *k_global,
+                                            const void *v_global, void *out, float *lse, int B,
+                                            int H, int N, int D, int window,
+                                            const int32_t *dilation, const int32_t *global_idx,
+                                            int n_global, float scale, sa_dtype dtype,
+                                            sa_stream_t stream) {
+  if (!q_global || !k_global || !v_global)
+    return fail(SA_ERR_INVALID_ARG, "q_global, k_global and v_global must be non-null");
+  return forward_impl(q, k, v, out, lse, B, H, N, D, window, dilation, global_idx, n_global,
+                      scale, dtype, reinterpret_cast<cudaStream_t>(stream), 0, 0, q_global,
+                      k_global, v_global);
 }
 
 extern "C" sa_status sa_count_pairs_chunked(int N, int n_memory, int chunk, int64_t *per_head) {

@@ -17,6 +17,10 @@ enum : int {
 
 struct DevProblem {
   const void *q, *k, *v;
+  // What the global-row pass reads: queries (gathered at the global
+  // positions), keys and values.  q, k, v themselves, or separate global
+  // projections of the same shape.
+  const void *gq_src, *gk_src, *gv_src;
   void *out;
   float *lse;       // [B*H*N] or null
   int N, D, H;

@@ -186,6 +186,9 @@ extern "C" sa_status sa_forward_noalloc(const void *q, const void *k, const void
   dp.q = q;
   dp.k = k;
   dp.v = v;
+  dp.gq_src = q;
+  dp.gk_src = k;
+  dp.gv_src = v;
   dp.out = out;
   dp.lse = lse;
   dp.N = N;

@@ -48,7 +48,7 @@ __global__ void gather_kernel(DevProblem p) {
   if (g < p.n_g) {
     const int64_t src = ((int64_t)bh * p.N + p.globals[g]) * p.D;
     for (int c = threadIdx.x; c < p.D; c += blockDim.x) {
-      static_cast<T *>(p.qg)[dst + c] = static_cast<const T *>(p.q)[src + c];
+      static_cast<T *>(p.qg)[dst + c] = static_cast<const T *>(p.gq_src)[src + c];
       static_cast<T *>(p.kg)[dst + c] = static_cast<const T *>(p.k)[src + c];
       static_cast<T *>(p.vg)[dst + c] = static_cast<const T *>(p.v)[src + c];
     }
@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(NT) global_simt_kernel(DevProblem p) {
 
   for (int t0 = key_lo; t0 < key_hi; t0 += KT) {
     __syncthreads();
-    load_rows<T, D>(Ks, p.k, base + (int64_t)t0 * D, D, min(KT, key_hi - t0));
-    load_rows<T, D>(Vs, p.v, base + (int64_t)t0 * D, D, min(KT, key_hi - t0));
+    load_rows<T, D>(Ks, p.gk_src, base + (int64_t)t0 * D, D, min(KT, key_hi - t0));
+    load_rows<T, D>(Vs, p.gv_src, base + (int64_t)t0 * D, D, min(KT, key_hi - t0));
     __syncthreads();
     simt_tile<D>(Qs, Ks, Vs, Ps, row, qd, p.scale_log2,
                  [&](int c) { return row_ok && t0 + c < key_hi; }, st_);

@@ -1148,8 +1148,9 @@ cudaError_t fill_common(tc::Params &P, const DevProblem &p, int BH) {
         (e = tc::make_map(&P.maps.qg, p.qg, D, p.g_pad, BH, D * 2, ghead, tc::kRows)))
       return e;
   }
-  if ((e = tc::make_map(&P.maps.kp, p.k, D, p.N, BH, D * 2, head, tc::kKeys)) ||
-      (e = tc::make_map(&P.maps.vp, p.v, D, p.N, BH, D * 2, head, tc::kKeys)))
+  // keys and values of the global-row pass
+  if ((e = tc::make_map(&P.maps.kp, p.gk_src, D, p.N, BH, D * 2, head, tc::kKeys)) ||
+      (e = tc::make_map(&P.maps.vp, p.gv_src, D, p.N, BH, D * 2, head, tc::kKeys)))
     return e;
   return cudaSuccess;
 }

@@ -46,6 +46,8 @@ SIGNATURES = {
                                 _F, _I, _VP]),
     "sa_forward_chunked": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _VP]),
     "sa_count_pairs_chunked": (_I, [_I, _I, _I, _I64P]),
+    "sa_forward_global_proj": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
+                                    _I32P, _I32P, _I, _F, _I, _VP]),
 }
 SA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -147,6 +149,44 @@ def forward(q, k, v, window: int, dilation: Sequence[int] | None = None,
             st = load().sa_forward_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                        lse.data_ptr(), B, H, N, D, int(window), _ptr(dil),
                                        _ptr(g), int(g.size), sc, dt, h_stream)
+    _check(st)
+    return out
+
+
+def forward_global_proj(q, k, v, q_global, k_global, v_global, window: int,
+                        dilation: Sequence[int] | None = None, globals_: Sequence[int] = (),
+                        scale: Optional[float] = None, out=None, lse=None, stream=None):
+    """Like ``forward``, with separate projections for the global attention
+    (sa_forward_global_proj): a global row scores ``q_global . k_global`` over
+    every key and averages ``v_global``; the other rows use q, k, v.  All six
+    inputs are contiguous CUDA tensors of one shape and dtype."""
+    import torch
+
+    dt = SA_BF16 if q.dtype == torch.bfloat16 else SA_FP32 if q.dtype == torch.float32 else None
+    if dt is None:
+        raise TypeError(f"unsupported dtype {q.dtype} (bfloat16 or float32)")
+    for t in (q, k, v, q_global, k_global, v_global):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or t.shape != q.shape:
+            raise ValueError("q, k, v and the global projections must be contiguous CUDA "
+                             "tensors of one shape and dtype")
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, D]")
+    B, H, N, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    dil = None if dilation is None else _i32(dilation)
+    if dil is not None and dil.size != H:
+        raise ValueError("dilation needs one entry per head")
+    g = _i32(globals_)
+    sc = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    with torch.cuda.device(q.device):
+        st = load().sa_forward_global_proj(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), q_global.data_ptr(), k_global.data_ptr(),
+            v_global.data_ptr(), out.data_ptr(), None if lse is None else lse.data_ptr(), B, H,
+            N, D, int(window), _ptr(dil), _ptr(g), int(g.size), sc, dt,
+            ctypes.c_void_p(stream.cuda_stream))
     _check(st)
     return out
 
