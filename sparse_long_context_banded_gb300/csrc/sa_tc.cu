@@ -462,81 +462,69 @@ struct Bars {
 // ---------------------------------------------------------------------------
 // softmax: one key tile of W columns for one row
 
-enum { kMaskNone = 0, kMaskInterval = 1, kMaskGlobal = 2 };
+// Masking of one key tile's scores (base-2 units; the scale's sign is applied
+// by the S product itself, which negates Q when the scale is negative, so the
+// softmax only ever sees a positive scale):
+//   every column is kept, or, when `interval` is set, columns [c_lo, c_hi]
+//   only (the window's edge tiles; a global tile keeps columns [0, c_hi], the
+//   globals it holds).  With `dedup`, a global tile also drops the globals
+//   already in the row's band (globals[g0 + x] is the global's class
+//   coordinate t_g, or kFarAway; the row is class position t_q; the global is
+//   in the row's band when |t_q - t_g| <= half, and is then counted once, as a
+//   band key).  One code path serves band and global tiles alike: the kernel's
+//   code has to stay small enough for the instruction caches of warps that
+//   run different roles on one sub-partition.
 
-// Masking of one key tile's scores (scores are in base-2 units; a negative
-// scale is applied to the scores themselves so that the maximum is taken on
-// scaled scores, a positive one is folded into the exponent):
-//   mode kMaskNone: every column.  kMaskInterval: columns [c_lo, c_hi].
-//   kMaskGlobal: columns <= c_hi whose global position is not already in the
-//   row's band (globals[g0 + x] is the global's class coordinate t_g, or
-//   kFarAway; the row is class position t_q; the global is in the row's band
-//   when |t_q - t_g| <= half, and is then counted once, as a band key).
-
-// W scores of this thread's row from TMEM, scaled and masked to -inf.
-template <int W>
-__device__ __forceinline__ void load_scores(uint32_t t_s, float neg_scale, int mode, int c_lo, int c_hi,
+// kKeys scores of this thread's row from TMEM, masked to -inf.
+__device__ __forceinline__ void load_scores(uint32_t t_s, bool interval, int c_lo, int c_hi,
                                             const int32_t *globals, int g0, int t_q, int half,
-                                            bool dedup, float (&s)[W]) {
+                                            bool dedup, float (&s)[kKeys]) {
   {
-    uint32_t r[W];
-    if constexpr (W == 128)
-      tmem_ld128(t_s, r);
-    else if constexpr (W == 64)
-      tmem_ld64(t_s, r);
-    else
-      tmem_ld32(t_s, r);
+    uint32_t r[kKeys];
+    tmem_ld128(t_s, r);
 #pragma unroll
-    for (int x = 0; x < W; ++x) s[x] = __uint_as_float(r[x]);
+    for (int x = 0; x < kKeys; ++x) s[x] = __uint_as_float(r[x]);
   }
-  if (neg_scale < 0.f) {
-#pragma unroll
-    for (int x = 0; x < W; ++x) s[x] *= neg_scale;
-  }
-  // band tiles (kKeys wide) take the interval mask, global tiles (kGKeys
-  // wide) the global one
   // branch-free: a compare and a select per column (the bounds differ per row)
-  if (W == kKeys && mode == kMaskInterval) {
+  if (interval) {
     const uint32_t span = (uint32_t)(c_hi - c_lo);
 #pragma unroll
-    for (int x = 0; x < W; ++x) {
+    for (int x = 0; x < kKeys; ++x) {
       const bool keep = (uint32_t)(x - c_lo) <= span;  // c_lo <= x <= c_hi
       s[x] = keep ? s[x] : -INFINITY;
     }
-  } else if (W == kGKeys && mode == kMaskGlobal) {
-    if (dedup) {
-      const uint32_t band = 2u * (uint32_t)half;
+  }
+  if (dedup) {
+    const uint32_t band = 2u * (uint32_t)half;
 #pragma unroll
-      for (int x = 0; x < W; ++x) {
-        // |t_q - t_g| > half, i.e. t_q - t_g + half outside [0, 2 half]; kFarAway
-        // (a global outside the class) is never in band
-        const bool out_of_band = (uint32_t)(t_q - globals[g0 + x] + half) > band;
-        const bool keep = (x <= c_hi) & out_of_band;
-        s[x] = keep ? s[x] : -INFINITY;
-      }
-    } else {
-#pragma unroll
-      for (int x = 0; x < W; ++x) s[x] = x <= c_hi ? s[x] : -INFINITY;
+    for (int x = 0; x < kGKeys; ++x) {
+      // |t_q - t_g| > half, i.e. t_q - t_g + half outside [0, 2 half]; kFarAway
+      // (a global outside the class) is never in band
+      const bool out_of_band = (uint32_t)(t_q - globals[g0 + x] + half) > band;
+      s[x] = out_of_band ? s[x] : -INFINITY;
     }
   }
 }
 
-// One key tile of W columns for one query row (this thread's TMEM lane): P =
+// One key tile for one query row (this thread's TMEM lane): P =
 // 2^(scale*S - m) as bf16 written over S, running maximum m and row sum l
 // updated, O in TMEM rescaled when the reference maximum moves.  The reference
 // maximum is raised only when the tile maximum exceeds it by more than 2^8, so
 // O is rescaled rarely; the same reference is used for P and for the running
-// sum, so the result is exact either way.  A 128-key tile is written in two
-// halves and announces the first (keys 0-63) on bar_half, so that the first
-// half of P V can start while the second half of P is computed.
-template <int W, int D>
-__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float scale, int mode,
+// sum, so the result is exact either way.  P is written in two halves of 64
+// keys and the first is announced on bar_half, so that the first half of P V
+// can start while the second half of P is computed; a global tile has 64 keys
+// (`narrow`) and only its first half is computed.
+template <int D>
+__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float scale, bool interval,
                                              int c_lo, int c_hi, const int32_t *globals, int g0,
-                                             int t_q, int half, bool dedup, uint32_t bar_half,
-                                             int lane, float &m_run, float &l_run) {
-  const float scl = scale < 0.f ? 1.f : scale;
+                                             int t_q, int half, bool dedup, bool narrow,
+                                             uint32_t bar_half, int lane, float &m_run,
+                                             float &l_run) {
+  constexpr int W = kKeys;
+  const float scl = scale;
   float s[W];
-  load_scores<W>(t_s, scale < 0.f ? scale : 0.f, mode, c_lo, c_hi, globals, g0, t_q, half, dedup, s);
+  load_scores(t_s, interval, c_lo, c_hi, globals, g0, t_q, half, dedup, s);
   // row maximum: eight chains of three-input max
   float mx[8];
 #pragma unroll
@@ -574,6 +562,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
   for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
+    if (hh == 1 && narrow) break;
     uint32_t pr[W / 4];
 #pragma unroll
     for (int j = 0; j < W / 4; ++j) {
@@ -583,11 +572,8 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
       sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
       pr[j] = pack_bf16(e.x, e.y);
     }
-    if constexpr (W == 128)
-      tmem_st32(t_s + hh * 32, pr);
-    else
-      tmem_st16(t_s + hh * 16, pr);
-    if (W == 128 && hh == 0) {
+    tmem_st32(t_s + hh * 32, pr);
+    if (hh == 0) {
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -763,8 +749,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     // execute.
     const int u = warp - 9;
     {
-      constexpr uint32_t kIdescS = idesc_bf16(kRows, kKeys, false);
-      constexpr uint32_t kIdescSg = idesc_bf16(kRows, kGKeys, false);
+      // a negative scale negates Q in the S products (bit 13: negate A)
+      const uint32_t neg_a = p.scale_log2 < 0.f ? (1u << 13) : 0u;
+      const uint32_t kIdescS = idesc_bf16(kRows, kKeys, false) | neg_a;
+      const uint32_t kIdescSg = idesc_bf16(kRows, kGKeys, false) | neg_a;
       constexpr uint32_t kIdescPV = idesc_bf16(kRows, D, true);
       const uint64_t dk_base = sw128_desc(s_slots, 16, 1024);
       const uint64_t dv_band = sw128_desc(s_slots, kKeys * 128, 1024);   // LBO: next 64 columns of V
@@ -896,7 +884,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     const uint32_t lane_addr = (uint32_t)((row >> 5) * 32) << 16;
     const uint32_t t_s = tmem + lane_addr + u * 128;
     const uint32_t t_o = tmem + lane_addr + 256 + u * 128;
-    const float sl = p.scale_log2;
+    // the S product carries the sign; a zero scale becomes a tiny one (every
+    // finite score then gives exactly 2^0, and a masked -inf stays -inf
+    // instead of turning into NaN)
+    const float sl = fmaxf(fabsf(p.scale_log2), 1e-30f);
     const int half = p.half;
     const int bar_id = 1 + u;
     int32_t *g_list = g_lists + u * SA_MAX_GLOBALS;
@@ -913,7 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
       const int ncnt_u = u ? w.n_cnt[1] : w.n_cnt[0];
       const int n = ncnt_u + w.ng;
       const int t_q = GLOBAL ? 0 : (w.q_tile + u) * kRows + row;  // class coordinate
-      if (!GLOBAL && w.ng > 0) {
+      if (!GLOBAL && w.ng > 0 && ((w.flags >> u) & 1)) {
+        // (only read by the in-band test of the global tile)
         // global positions in this item's residue-class coordinates: g = r + d*t
         // gives t; a global outside the class can never lie in a row's band.
         // (The previous item's readers of this list passed the warpgroup's
@@ -932,12 +924,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
         ++scnt;
         if (!ok) break;
         tc_fence_after();
+        bool interval = true;
+        int c_lo = 0, c_hi, g0 = 0;
         if (!gt) {
           const int kb = GLOBAL ? (w.key0 + band_index(w, pos) * kKeys) : (w.lo + band_index(w, pos)) * kKeys;
-          bool full;
-          int c_lo = 0, c_hi = kKeys - 1;
           if (GLOBAL) {
-            full = kb + kKeys <= w.key_end;
+            interval = kb + kKeys > w.key_end;
             c_hi = w.key_end - 1 - kb;
           } else {
             // the tile is full when every row's key interval covers it; the
@@ -947,26 +939,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
             int lo_last, hi_first, r_lo, r_hi, unused;
             row_keys(half, p.chunk, p.memory, w.len, q0 + kRows - 1, lo_last, unused);
             row_keys(half, p.chunk, p.memory, w.len, q0, unused, hi_first);
-            full = lo_last <= kb && hi_first >= kb + kKeys - 1;
+            interval = !(lo_last <= kb && hi_first >= kb + kKeys - 1);
             row_keys(half, p.chunk, p.memory, w.len, t_q, r_lo, r_hi);
             c_lo = r_lo - kb;
             c_hi = r_hi - kb;
           }
-          softmax_tile<kKeys, D>(t_s, t_o, sl, full ? kMaskNone : kMaskInterval, c_lo, c_hi, nullptr,
-                                 0, 0, 0, false, B.p_half + 8 * u, lane, m_run, l_run);
         } else {
-          const int g0 = global_index(w, pos) * kGKeys;
-          const bool dedup = (w.flags >> u) & 1;
-          softmax_tile<kGKeys, D>(t_s, t_o, sl, kMaskGlobal, 0, p.n_g - 1 - g0, g_list, g0, t_q,
-                                  half, dedup, B.p_half + 8 * u, lane, m_run, l_run);
+          // a global tile holds kGKeys gathered keys; the columns past them
+          // (and past the last global) are masked
+          g0 = global_index(w, pos) * kGKeys;
+          c_hi = min(p.n_g - 1 - g0, kGKeys - 1);
         }
+        softmax_tile<D>(t_s, t_o, sl, interval, c_lo, c_hi, g_list, g0, t_q, half,
+                        gt && ((w.flags >> u) & 1), gt, B.p_half + 8 * u, lane, m_run, l_run);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          if (gt) mbar_arrive(B.p_half + 8 * u);  // a global tile is written in one piece
-          mbar_arrive(B.p_full + 8 * u);
-        }
+        if (lane == 0) mbar_arrive(B.p_full + 8 * u);
       }
 
       // every thread of the warpgroup takes part in the same barriers, so the

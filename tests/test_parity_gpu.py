@@ -87,6 +87,33 @@ def test_small_full(case, oracle):
     assert_lse_close(got_lse, ref_lse, str(case))
 
 
+# A scale several times 1/sqrt(D) makes each row's softmax peak on a few keys,
+# where the bf16 rounding of P no longer averages out (as for rows with few
+# keys); such scales run through the fp32 path.
+SCALE_CASES = [
+    # B, H, N, D, window, dilation, globals, dtype, scale
+    (1, 2, 1000, 128, 256, [1, 2], [0, 999], "bf16", -0.0883),   # negative scale
+    (1, 1, 700, 64, 300, [1], [3], "bf16", -0.125),
+    (1, 1, 700, 64, 300, [1], [3], "fp32", -1.0),
+    (1, 2, 515, 64, 200, [1, 1], [0], "fp32", -0.125),
+    (1, 1, 640, 128, 128, [1], [0, 1], "bf16", 0.0),             # zero scale: plain averages
+    (1, 1, 640, 64, 128, [1], [0, 1], "fp32", 0.0),
+    (1, 1, 640, 64, 128, [1], [5], "bf16", 0.2),
+    (1, 1, 640, 64, 128, [1], [5], "fp32", 0.6),                 # large positive scale
+]
+
+
+@pytest.mark.parametrize("case", SCALE_CASES, ids=lambda c: "N{}D{}s{}{}".format(
+    c[2], c[3], c[8], c[7]))
+def test_scale_sign_and_size(case, oracle):
+    B, H, N, D, window, dil, G, dtype, scale = case
+    q, k, v = make(B, H, N, D, dtype, seed=zlib.crc32(repr(case).encode()))
+    got, got_lse = run_gpu(q, k, v, window, dil, G, scale)
+    ref, ref_lse = oracle.forward_longformer(q, k, v, window, dil, G, scale=scale)
+    assert_close(got, ref, str(case))
+    assert_lse_close(got_lse, ref_lse, str(case))
+
+
 def sample_rows(w, rng, n_random):
     """Flattened row ids covering tile seams, the tail, globals and random rows."""
     rows = set()
