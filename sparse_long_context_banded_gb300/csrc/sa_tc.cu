@@ -4,19 +4,18 @@
 // What one CTA computes (Unlimiformer section 2.3 Eq. (1) under the additive
 // {0,-inf} mask of GMAT's "Global-Memory Augmented Transformers" section):
 // two 128-row query tiles Q_0, Q_1, each against its own list of key tiles --
-// the gathered global keys (Longformer glossary, "How the Longformer attention
-// works": global attention; GMAT "Global Memory") followed by the band tiles
-// that intersect its rows' windows (the same section's sliding / dilated
-// window) -- with an exact online softmax in fp32.  The global tiles come first
-// because both query tiles read them: the two tiles' MMAs overlap from the
-// start of an item, and the next item's first loads depend only on slots the
-// current item released early.
+// the band tiles that intersect its rows' windows (Longformer glossary, "How
+// the Longformer attention works": sliding / dilated window) followed by the
+// gathered global keys (the same section's global attention; GMAT "Global
+// Memory") -- with an exact online softmax in fp32.  The two query tiles are
+// neighbours, so their band lists overlap and each key/value tile is loaded
+// once for both.
 //
-//   S = Q_u K_j^T (tcgen05, fp32 in TMEM) -> scale, mask (edge tiles only),
-//   running max / sum per row -> P = exp2(S - m) as bf16 written back into the
-//   same TMEM columns, in two halves -> O_u += P V_j (tcgen05, A operand from
-//   TMEM; the first half of the product starts once the first half of P is in
-//   place).
+//   S = Q_u K_j^T (tcgen05, fp32 in TMEM; Q negated for a negative scale) ->
+//   mask (edge tiles only), running max / sum per row -> P = exp2(scale S - m)
+//   as bf16 written back into the same TMEM columns, in two halves -> O_u +=
+//   P V_j (tcgen05, A operand from TMEM; the first half of the product starts
+//   once the first half of P is in place).
 //
 // In global mode the two query tiles are the gathered global rows and the key
 // tiles one chunk of all N keys; the CTA writes unnormalised partial outputs
