@@ -94,6 +94,8 @@ class Oracle:
             ctypes.c_void_p] * 6 + [ctypes.c_int] * 6 + [i32p, i32p, ctypes.c_int] + tail
         lib.oracle_forward_longformer_global_proj.restype = ctypes.c_int
         lib.oracle_forward_gmat.restype = ctypes.c_int
+        lib.oracle_forward_gather.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 7 + tail
+        lib.oracle_forward_gather.restype = ctypes.c_int
         self.lib = lib
 
     # -- global set --------------------------------------------------------
@@ -229,6 +231,45 @@ class Oracle:
         if rows is None:
             out = out.reshape(B, H, N, D)
             lse = None if lse is None else lse.reshape(B, H, N)
+        return out, lse
+
+
+    def forward_gather(self, q, k, v, idx, scale: float | None = None, rows=None,
+                       threads: int | None = None, want_lse: bool = True):
+        """Attention over per-query key lists, fp64 (Unlimiformer, sections 2.2-2.3).
+
+        q: [B, H, Nq, D]; k, v: [B, H, Nk, D] (one dtype); idx: int32
+        [B, H, Nq, K], row i of head (b, h) scoring the keys it lists; entries
+        outside [0, Nk) are padding, a repeated entry counts once per listing.
+        Returns (out [B,H,Nq,D] or [n_rows,D], lse [B,H,Nq] or [n_rows]); a row
+        with no valid entry gives 0 and -inf.
+        """
+        arrs = [np.ascontiguousarray(a) for a in (q, k, v)]
+        code = _DTYPE_CODE.get(arrs[0].dtype)
+        if code is None or any(a.dtype != arrs[0].dtype for a in arrs):
+            raise TypeError("q, k, v must share one dtype: uint16 (bf16 bits), float32 or float64")
+        q, k, v = arrs
+        if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] \
+                or q.shape[3] != k.shape[3]:
+            raise ValueError("q must be [B, H, Nq, D] and k, v [B, H, Nk, D]")
+        B, H, Nq, D = q.shape
+        Nk = k.shape[2]
+        idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int32))
+        if idx.ndim != 4 or idx.shape[:3] != (B, H, Nq):
+            raise ValueError("idx must be [B, H, Nq, K]")
+        K = idx.shape[3]
+        sc = float(scale if scale is not None else 1.0 / np.sqrt(D))
+        r, n = self._rows(rows, B * H * Nq)
+        out = np.empty((n, D), dtype=np.float64)
+        lse = np.empty(n, dtype=np.float64) if want_lse else None
+        rc = self.lib.oracle_forward_gather(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(idx), code, B, H, Nq, Nk, D, K, sc, _ptr(r),
+            int(n), _ptr(out), _ptr(lse), int(threads or default_threads()))
+        if rc:
+            raise MemoryError("oracle forward failed")
+        if rows is None:
+            out = out.reshape(B, H, Nq, D)
+            lse = None if lse is None else lse.reshape(B, H, Nq)
         return out, lse
 
 

@@ -499,3 +499,141 @@ int oracle_forward_gmat(const void *q, const void *k, const void *v, int dtype,
   return run_forward(&ms, q, k, v, NULL, NULL, NULL, dtype, B, H, N, D, scale, rows,
                      n_rows, out, lse, threads);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Attention over per-query key lists ("Unlimiformer", section 2.2
+ * "Retrieval-augmented Cross-Attention" and section 2.3 Eq. (1): each query
+ * attends only to the keys its retrieval returned, with the standard
+ * dot-product attention over that set).                                     */
+/*
+ * q: [B, H, Nq, D]; k, v: [B, H, Nk, D]; idx: int32 [B, H, Nq, K] -- row i of
+ * head (b, h) scores exactly the keys listed in idx[b][h][i][0..K).  Readings
+ * (the pages describe retrieval of a top-k set and say nothing of ragged or
+ * repeated lists):
+ *   - an entry outside [0, Nk) (e.g. -1) is padding and is skipped;
+ *   - the list is a sum: an index listed twice is counted twice (a top-k list
+ *     has no repeats, so nothing changes for retrieval output);
+ *   - a row whose list has no valid entry has output 0 and log-sum-exp -inf.
+ * Per row, in double:
+ *   s_t = scale * q_i . k_{idx_t}  for each valid entry t,  m = max_t s_t,
+ *   o_i = sum_t exp(s_t - m) v_{idx_t} / sum_t exp(s_t - m),
+ *   lse_i = m + log(sum_t exp(s_t - m)).
+ */
+typedef struct {
+  const void *q, *k, *v;
+  const int32_t *idx;
+  int dtype;
+  int H, Nq, Nk, D, K;
+  double scale;
+  const int64_t *rows; /* flattened (b*H + h)*Nq + i, or NULL for all rows */
+  double *out, *lse;
+  int64_t begin, end;
+  int status;
+} gather_job;
+
+/* Is list entry j a key of the head (not padding)? */
+static int gather_valid(int j, int Nk) { return j >= 0 && j < Nk; }
+
+static void *gather_worker(void *arg) {
+  gather_job *job = (gather_job *)arg;
+  int D = job->D, K = job->K;
+  double *s = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+  double *qi = (double *)malloc(sizeof(double) * (size_t)D);
+  int64_t r;
+  job->status = 0;
+  if (!s || !qi) {
+    job->status = -1;
+    free(s);
+    free(qi);
+    return NULL;
+  }
+  for (r = job->begin; r < job->end; ++r) {
+    int64_t flat = job->rows ? job->rows[r] : r;
+    int64_t bh = flat / job->Nq;
+    int64_t qbase = flat * D;                    /* this query row */
+    int64_t kbase = bh * (int64_t)job->Nk * D;   /* this head's keys and values */
+    const int32_t *list = job->idx + flat * K;
+    double top = -INFINITY, total = 0.0;
+    double *o = job->out + r * (int64_t)D;
+    int t, d, n_valid = 0;
+    for (d = 0; d < D; ++d) qi[d] = load_elem(job->q, job->dtype, qbase + d);
+    /* scores of the listed keys, and their maximum */
+    for (t = 0; t < K; ++t) {
+      double dot = 0.0;
+      if (!gather_valid(list[t], job->Nk)) continue;
+      for (d = 0; d < D; ++d)
+        dot += qi[d] * load_elem(job->k, job->dtype, kbase + (int64_t)list[t] * D + d);
+      s[t] = job->scale * dot;
+      if (s[t] > top) top = s[t];
+      ++n_valid;
+    }
+    for (d = 0; d < D; ++d) o[d] = 0.0;
+    if (n_valid == 0) {
+      if (job->lse) job->lse[r] = -INFINITY;
+      continue;
+    }
+    /* weights, normaliser and weighted sum of the listed values */
+    for (t = 0; t < K; ++t) {
+      double w;
+      if (!gather_valid(list[t], job->Nk)) continue;
+      w = exp(s[t] - top);
+      total += w;
+      for (d = 0; d < D; ++d)
+        o[d] += w * load_elem(job->v, job->dtype, kbase + (int64_t)list[t] * D + d);
+    }
+    for (d = 0; d < D; ++d) o[d] = o[d] / total;
+    if (job->lse) job->lse[r] = top + log(total);
+  }
+  free(s);
+  free(qi);
+  return NULL;
+}
+
+/* rows == NULL computes every row into out[B*H*Nq][D]; otherwise only the
+ * listed flattened rows, in order.  Returns 0 or -1. */
+int oracle_forward_gather(const void *q, const void *k, const void *v, const int32_t *idx,
+                          int dtype, int B, int H, int Nq, int Nk, int D, int K,
+                          double scale, const int64_t *rows, int64_t n_rows, double *out,
+                          double *lse, int threads) {
+  gather_job *jobs;
+  pthread_t *tids;
+  int64_t total = rows ? n_rows : (int64_t)B * H * Nq, per;
+  int t, status = 0;
+  if (threads < 1) threads = 1;
+  if (total < threads) threads = total > 0 ? (int)total : 1;
+  jobs = (gather_job *)calloc((size_t)threads, sizeof(gather_job));
+  tids = (pthread_t *)calloc((size_t)threads, sizeof(pthread_t));
+  if (!jobs || !tids) {
+    free(jobs);
+    free(tids);
+    return -1;
+  }
+  per = (total + threads - 1) / threads;
+  for (t = 0; t < threads; ++t) {
+    gather_job *job = &jobs[t];
+    job->q = q;
+    job->k = k;
+    job->v = v;
+    job->idx = idx;
+    job->dtype = dtype;
+    job->H = H;
+    job->Nq = Nq;
+    job->Nk = Nk;
+    job->D = D;
+    job->K = K;
+    job->scale = scale;
+    job->rows = rows;
+    job->out = out;
+    job->lse = lse;
+    job->begin = (int64_t)t * per < total ? (int64_t)t * per : total;
+    job->end = (int64_t)(t + 1) * per < total ? (int64_t)(t + 1) * per : total;
+    pthread_create(&tids[t], NULL, gather_worker, job);
+  }
+  for (t = 0; t < threads; ++t) {
+    pthread_join(tids[t], NULL);
+    if (jobs[t].status) status = -1;
+  }
+  free(jobs);
+  free(tids);
+  return status;
+}

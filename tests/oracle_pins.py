@@ -301,10 +301,88 @@ def pin_bf16_decode(o):
     assert np.array_equal(out, np.full((1, 1, 2, 2), 1.5))
 
 
+def _lists_to_mask(idx, Nk):
+    """Additive float mask from key lists: log(count) where listed, -inf elsewhere
+    (entries outside [0, Nk) ignored)."""
+    B, H, Nq, K = idx.shape
+    cnt = np.zeros((B, H, Nq, Nk))
+    for b in range(B):
+        for h in range(H):
+            for i in range(Nq):
+                for j in idx[b, h, i]:
+                    if 0 <= j < Nk:
+                        cnt[b, h, i, j] += 1
+    with np.errstate(divide="ignore"):
+        return np.log(cnt), cnt
+
+
+def pin_gather_dense(o):
+    """Per-query lists holding every key (each in its own shuffled order) give
+    dense softmax attention of q over k, v (SDPA, fp64), and the log-sum-exp of
+    the scaled score matrix (matmul + logsumexp)."""
+    rng = np.random.default_rng(21)
+    B, H, Nq, Nk, D = 1, 2, 9, 23, 16
+    q, k, v = randn((B, H, Nq, D), 1), randn((B, H, Nk, D), 2), randn((B, H, Nk, D), 3)
+    idx = np.stack([np.stack([np.stack([rng.permutation(Nk) for _ in range(Nq)])
+                              for _ in range(H)]) for _ in range(B)]).astype(np.int32)
+    out, lse = o.forward_gather(q, k, v, idx, scale=0.3)
+    assert np.allclose(out, sdpa(q, k, v, None, 0.3), rtol=1e-11, atol=1e-12)
+    sc = 0.3 * np.einsum("bhid,bhjd->bhij", q, k)
+    ref_lse = sc.max(-1) + np.log(np.exp(sc - sc.max(-1, keepdims=True)).sum(-1))
+    assert np.allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+
+
+def pin_gather_lists_with_padding_and_repeats(o):
+    """Ragged lists (padding -1 and indices >= Nk skipped) with repeated entries:
+    the same as SDPA with an additive mask of log(times listed) -- a key listed
+    twice weighs twice -- and rows with no valid entry give 0 and -inf."""
+    rng = np.random.default_rng(22)
+    B, H, Nq, Nk, D, K = 2, 2, 11, 30, 8, 12
+    q, k, v = randn((B, H, Nq, D), 4), randn((B, H, Nk, D), 5), randn((B, H, Nk, D), 6)
+    idx = rng.integers(0, Nk, size=(B, H, Nq, K)).astype(np.int32)
+    idx[rng.random(idx.shape) < 0.2] = -1
+    idx[rng.random(idx.shape) < 0.05] = Nk + 3
+    idx[0, 1, 4] = -1                         # an empty row
+    idx[1, 0, 2, :3] = [7, 7, 7]             # one key three times
+    mask, cnt = _lists_to_mask(idx, Nk)
+    assert cnt.max() >= 3
+    out, lse = o.forward_gather(q, k, v, idx, scale=0.5)
+    t = [torch.from_numpy(np.asarray(a, dtype=np.float64)) for a in (q, k, v)]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        *t, attn_mask=torch.from_numpy(mask), scale=0.5).numpy()
+    has = cnt.sum(-1) > 0
+    assert np.allclose(out[has], ref[has], rtol=1e-11, atol=1e-12)
+    assert (out[~has] == 0).all() and np.isneginf(lse[~has]).all() and (~has).sum() == 1
+    sc = 0.5 * np.einsum("bhid,bhjd->bhij", q, k) + mask
+    m = sc.max(-1)
+    ref_lse = m + np.log(np.exp(sc - m[..., None]).sum(-1))
+    assert np.allclose(lse[has], ref_lse[has], rtol=1e-12, atol=1e-12)
+
+
+def pin_gather_band_is_longformer(o):
+    """The Longformer pattern written as per-row key lists gives the mask-based
+    Longformer forward (two code paths of the oracle that share no mask code),
+    per head with different dilations."""
+    N, D, w, dil, G = 57, 8, 12, [1, 3], [0, 20]
+    q, k, v = (randn((1, 2, N, D), 70 + s) for s in range(3))
+    masks = [o.mask_longformer(N, w, d, G) for d in dil]
+    K = max(int(m.sum(1).max()) for m in masks)
+    idx = np.full((1, 2, N, K), -1, dtype=np.int32)
+    for h, m in enumerate(masks):
+        for i in range(N):
+            js = np.flatnonzero(m[i])[::-1]  # any order
+            idx[0, h, i, :js.size] = js
+    got, got_lse = o.forward_gather(q, k, v, idx, scale=0.25)
+    ref, ref_lse = o.forward_longformer(q, k, v, w, dil, G, scale=0.25)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-13)
+    assert np.allclose(got_lse, ref_lse, rtol=1e-12, atol=1e-13)
+
+
 ALL_PINS = [
     pin_page_printed_counts, pin_closed_form_counts, pin_brute_force_masks,
     pin_brute_force_attention, pin_dense_limit, pin_global_rows_dense,
     pin_gmat_band_is_longformer_with_memory_globals, pin_memory_permutation,
     pin_shift_invariance, pin_dilation_is_band_per_residue, pin_chunked,
-    pin_bf16_decode, pin_global_projections,
+    pin_bf16_decode, pin_global_projections, pin_gather_dense,
+    pin_gather_lists_with_padding_and_repeats, pin_gather_band_is_longformer,
 ]

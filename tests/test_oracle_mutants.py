@@ -35,6 +35,19 @@ MUTANTS = {
                                 "row[j] = (uint8_t)(((i - M + 1) / C) == ((j - M) / C));"),
     "bf16_decode_shift": ("uint32_t wide = ((uint32_t)bits) << 16;",
                           "uint32_t wide = ((uint32_t)bits) << 15;"),
+    "gather_scale_dropped": ("s[t] = job->scale * dot;", "s[t] = dot;"),
+    "gather_value_from_keys": (
+        "o[d] += w * load_elem(job->v, job->dtype, kbase + (int64_t)list[t] * D + d);",
+        "o[d] += w * load_elem(job->k, job->dtype, kbase + (int64_t)list[t] * D + d);"),
+    "gather_first_query_of_head": ("int64_t qbase = flat * D;",
+                                   "int64_t qbase = bh * (int64_t)job->Nq * D;"),
+    "gather_head_offset_dropped": ("int64_t kbase = bh * (int64_t)job->Nk * D;",
+                                   "int64_t kbase = 0;"),
+    "gather_lse_without_max": ("job->lse[r] = top + log(total);",
+                               "job->lse[r] = log(total);"),
+    "gather_repeats_counted_once": (
+        "      if (!gather_valid(list[t], job->Nk)) continue;\n      w = exp(s[t] - top);",
+        "      if (!gather_valid(list[t], job->Nk)) continue;\n      if (t > 0 && list[t] == list[t - 1]) continue;\n      w = exp(s[t] - top);"),
 }
 
 
