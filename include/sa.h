@@ -162,6 +162,37 @@ sa_status sa_forward_chunked(const void *q, const void *k, const void *v, void *
  */
 sa_status sa_count_pairs_chunked(int N, int n_memory, int chunk, int64_t *per_head);
 
+/*
+ * sa_forward_gather -- attention over per-query key lists ("Unlimiformer:
+ * Long-Range Transformers with Unlimited Length Input", section 2.2
+ * "Retrieval-augmented Cross-Attention": each head retrieves the top-k keys of
+ * a query and attends only to them; section 2.3 Eq. (1): standard dot-product
+ * attention over that set).  The retrieval (a kNN index) is the caller's; this
+ * call takes its result.  Row i of head (b, h):
+ *   out[b,h,i] = sum_t softmax_t(scale * <q[b,h,i], k[b,h,idx_t]>) v[b,h,idx_t]
+ * over the valid entries idx_t = idx[b,h,i,t], t < K.
+ *
+ *  q         device, [B,H,Nq,D] in `dtype`; read only.
+ *  k, v      device, [B,H,Nk,D] in `dtype`; read only.
+ *  idx       device, int32 [B,H,Nq,K]; read only.  An entry outside [0, Nk)
+ *            (e.g. -1) is padding and is skipped, so lists may be ragged; an
+ *            index listed twice counts twice (retrieval output has no repeats).
+ *            May be NULL when K == 0.
+ *  out       device, [B,H,Nq,D] in `dtype`; fully written.  A row with no valid
+ *            entry gets zeros.
+ *  lse       device, float32 [B,H,Nq], or NULL: natural-log log-sum-exp of the
+ *            row's scores (-inf for a row with no valid entry).
+ *  B, H, Nq, Nk >= 1; K >= 0; D: 64 or 128 (else SA_ERR_UNSUPPORTED).
+ *  scale     finite.  dtype: SA_BF16 or SA_FP32 (fp32 arithmetic either way).
+ *  q, k, v, out 16-byte aligned; idx, lse 4-byte aligned.
+ *  Errors: SA_ERR_INVALID_ARG / SA_ERR_UNSUPPORTED before any launch;
+ *  SA_ERR_CUDA if the launch fails.  Asynchronous on `stream`; allocates no
+ *  device memory.  Timed as stage 1 by sa_profile_begin/end.
+ */
+sa_status sa_forward_gather(const void *q, const void *k, const void *v, const int32_t *idx,
+                            void *out, float *lse, int B, int H, int Nq, int Nk, int D, int K,
+                            float scale, sa_dtype dtype, sa_stream_t stream);
+
 /* Thread-local description of the last non-OK status on this host thread. */
 const char *sa_last_error(void);
 
@@ -177,8 +208,9 @@ sa_status sa_sync_status(sa_stream_t stream);
  * sa_forward* call records CUDA events around each of its kernel launches on
  * its own stream.  sa_profile_end() waits for those events and returns, per
  * stage, the number of launches and their summed device time in milliseconds.
- * Stages: 0 gather of global rows, 1 band tiles, 2 global-row split-K pass,
- * 3 merge of partial softmax statistics.  Process-wide; not for concurrent use
+ * Stages: 0 gather of global rows, 1 band tiles (or the list attention of
+ * sa_forward_gather), 2 global-row split-K pass, 3 merge of partial softmax
+ * statistics.  Process-wide; not for concurrent use
  * from several threads.
  */
 #define SA_NUM_STAGES 4

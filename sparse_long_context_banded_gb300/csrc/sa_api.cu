@@ -397,6 +397,45 @@ extern "C" sa_status sa_forward_global_proj(const void *q, const void *k, const 
                       k_global, v_global);
 }
 
+extern "C" sa_status sa_forward_gather(const void *q, const void *k, const void *v,
+                                       const int32_t *idx, void *out, float *lse, int B, int H,
+                                       int Nq, int Nk, int D, int K, float scale,
+                                       sa_dtype dtype, sa_stream_t stream) {
+  if (!q || !k || !v || !out) return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be non-null");
+  if (K > 0 && !idx) return fail(SA_ERR_INVALID_ARG, "idx is null but K = %d", K);
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1)
+    return fail(SA_ERR_INVALID_ARG, "B, H, Nq and Nk must be >= 1 (got %d, %d, %d, %d)", B, H, Nq, Nk);
+  if (K < 0) return fail(SA_ERR_INVALID_ARG, "K must be >= 0 (got %d)", K);
+  if (!std::isfinite(scale)) return fail(SA_ERR_INVALID_ARG, "scale must be finite");
+  if (dtype != SA_BF16 && dtype != SA_FP32) return fail(SA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  const void *ptrs[4] = {q, k, v, out};
+  for (int i = 0; i < 4; ++i)
+    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0)
+      return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(idx) % 4 != 0 || reinterpret_cast<uintptr_t>(lse) % 4 != 0)
+    return fail(SA_ERR_INVALID_ARG, "idx and lse must be 4-byte aligned");
+  if (D != 64 && D != 128) return fail(SA_ERR_UNSUPPORTED, "D = %d (supported: 64, 128)", D);
+  GatherProblem gp{};
+  gp.q = q;
+  gp.k = k;
+  gp.v = v;
+  gp.idx = idx;
+  gp.out = out;
+  gp.lse = lse;
+  gp.rows = (int64_t)B * H * Nq;
+  gp.Nq = Nq;
+  gp.Nk = Nk;
+  gp.K = K;
+  gp.D = D;
+  gp.scale_log2 = scale * 1.4426950408889634f;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  StageTimer timer(1, s);
+  cudaError_t e = launch_gather_attention(gp, dtype, s);
+  timer.done();
+  if (e != cudaSuccess) return cuda_fail(e, "list-gather attention launch");
+  return SA_OK;
+}
+
 extern "C" sa_status sa_count_pairs_chunked(int N, int n_memory, int chunk, int64_t *per_head) {
   if (N < 1) return fail(SA_ERR_INVALID_ARG, "N must be >= 1 (got %d)", N);
   if (chunk < 1) return fail(SA_ERR_INVALID_ARG, "chunk must be >= 1 (got %d)", chunk);

@@ -42,6 +42,18 @@ struct DevProblem {
   int *err;
 };
 
+// Attention over per-query key lists (sa_gather.cu).
+struct GatherProblem {
+  const void *q, *k, *v;  // [B*H][Nq][D], [B*H][Nk][D], [B*H][Nk][D]
+  const int32_t *idx;     // [B*H][Nq][K]; entries outside [0, Nk) are padding
+  void *out;              // [B*H][Nq][D]
+  float *lse;             // [B*H][Nq] or null
+  int64_t rows;           // B*H*Nq
+  int Nq, Nk, K, D;
+  float scale_log2;
+};
+cudaError_t launch_gather_attention(const GatherProblem &p, sa_dtype dt, cudaStream_t s);
+
 // SIMT path (fp32 inputs): CUDA-core arithmetic, fp32 throughout.
 constexpr Tiling kSimtTiling{64, 1, 64, 64, 64, 608, 1 << 30};
 cudaError_t launch_gather(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s);

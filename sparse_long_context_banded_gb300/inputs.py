@@ -14,6 +14,14 @@ described on):
   * the scattered-globals workload draws its 32 global positions with
     ``default_rng(2000 + c).choice(N, 32, replace=False)`` and sorts them.
   * scale = 1/sqrt(D).
+
+Attention over per-query key lists (the retrieval form: each query attends to
+the top-k keys a kNN index returned) has its own recipe, since the pages give
+no datastore and no index: q [B, H, Nq, D] and k, v [B, H, Nk, D] are drawn as
+above from ``default_rng(3000 + seed)``; each query's list holds K positions
+drawn uniformly from [0, Nk) by the same generator, sorted ascending, with every
+draw that repeats an earlier one turned into padding (-1) -- distinct keys, as
+a top-k list has, and slightly ragged lists.
 """
 from __future__ import annotations
 
@@ -114,3 +122,46 @@ def draw_qkv(w: Workload, seed: Optional[int] = None):
         x = rng.standard_normal(shape, dtype=np.float32)
         out.append(bf16_bits(x) if w.dtype == "bf16" else x)
     return tuple(out)
+
+
+@dataclasses.dataclass(frozen=True)
+class GatherWorkload:
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    D: int
+    K: int          # list length per query
+    dtype: str      # "fp32" or "bf16"
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def describe(self) -> str:
+        return (f"{self.name}: B={self.B} H={self.H} Nq={self.Nq} Nk={self.Nk} D={self.D} "
+                f"K={self.K} {self.dtype}")
+
+
+def gather_workload() -> GatherWorkload:
+    """Retrieval attention at long-context scale: 4096 queries per head, each
+    attending to 1024 of a 131072-key datastore (the top-k width the
+    Unlimiformer page uses is the model's context window)."""
+    return GatherWorkload("retrieval attention", 1, 16, 4096, 131072, 128, 1024, "bf16")
+
+
+def draw_gather(w: GatherWorkload, seed: int = 0):
+    """(q, k, v, idx): q, k, v as in draw_qkv (uint16 bf16 bits or float32),
+    idx int32 [B, H, Nq, K] (see the module docstring)."""
+    rng = np.random.default_rng(3000 + seed)
+    arrs = []
+    for shape in ((w.B, w.H, w.Nq, w.D), (w.B, w.H, w.Nk, w.D), (w.B, w.H, w.Nk, w.D)):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        arrs.append(bf16_bits(x) if w.dtype == "bf16" else x)
+    idx = np.sort(rng.integers(0, w.Nk, size=(w.B, w.H, w.Nq, w.K), dtype=np.int32), axis=-1)
+    if w.K > 1:
+        rep = np.zeros(idx.shape, dtype=bool)
+        rep[..., 1:] = idx[..., 1:] == idx[..., :-1]
+        idx[rep] = -1
+    return tuple(arrs) + (idx,)

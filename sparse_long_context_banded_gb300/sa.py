@@ -46,6 +46,8 @@ SIGNATURES = {
                                 _F, _I, _VP]),
     "sa_forward_chunked": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _VP]),
     "sa_count_pairs_chunked": (_I, [_I, _I, _I, _I64P]),
+    "sa_forward_gather": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I,
+                               _VP]),
     "sa_forward_global_proj": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                     _I32P, _I32P, _I, _F, _I, _VP]),
 }
@@ -186,6 +188,42 @@ def forward_global_proj(q, k, v, q_global, k_global, v_global, window: int,
             q.data_ptr(), k.data_ptr(), v.data_ptr(), q_global.data_ptr(), k_global.data_ptr(),
             v_global.data_ptr(), out.data_ptr(), None if lse is None else lse.data_ptr(), B, H,
             N, D, int(window), _ptr(dil), _ptr(g), int(g.size), sc, dt,
+            ctypes.c_void_p(stream.cuda_stream))
+    _check(st)
+    return out
+
+
+def forward_gather(q, k, v, idx, scale: Optional[float] = None, out=None, lse=None,
+                   stream=None):
+    """Attention of each query row over the keys its list names
+    (sa_forward_gather).  q: [B, H, Nq, D]; k, v: [B, H, Nk, D] (CUDA,
+    bfloat16 or float32, contiguous); idx: int32 CUDA tensor [B, H, Nq, K]
+    (entries outside [0, Nk) are padding).  Returns ``out`` [B, H, Nq, D]."""
+    import torch
+
+    dt = SA_BF16 if q.dtype == torch.bfloat16 else SA_FP32 if q.dtype == torch.float32 else None
+    if dt is None:
+        raise TypeError(f"unsupported dtype {q.dtype} (bfloat16 or float32)")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or t.dim() != 4:
+            raise ValueError("q, k, v must be contiguous 4-d CUDA tensors of one dtype")
+    B, H, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[:2] != (B, H) or k.shape[3] != D:
+        raise ValueError("k and v must be [B, H, Nk, D] with q's B, H and D")
+    Nk = k.shape[2]
+    if (idx.dtype != torch.int32 or not idx.is_cuda or not idx.is_contiguous()
+            or idx.dim() != 4 or tuple(idx.shape[:3]) != (B, H, Nq)):
+        raise ValueError("idx must be a contiguous int32 CUDA tensor [B, H, Nq, K]")
+    K = idx.shape[3]
+    if out is None:
+        out = torch.empty_like(q)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sc = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    with torch.cuda.device(q.device):
+        st = load().sa_forward_gather(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), idx.data_ptr() if K else None,
+            out.data_ptr(), None if lse is None else lse.data_ptr(), B, H, Nq, Nk, D, K, sc, dt,
             ctypes.c_void_p(stream.cuda_stream))
     _check(st)
     return out
