@@ -74,6 +74,14 @@ def peaks():
             "source": "fallback"}
 
 
+# DRAM bytes (read + write) of one band-kernel launch per head of the
+# long-context workload: ncu dram__bytes_read.sum + dram__bytes_write.sum of the
+# 2-head capture in profiles/band_kernel_long_context_h2.md (260.4 MB), halved.
+# Heads are independent slices of the same work, so a launch over H heads moves
+# H times this.  Valid for the kernel build that capture was taken of.
+BAND_DRAM_BYTES_PER_HEAD = (217_097_216 + 43_269_120) / 2
+
+
 def workload_flops(w, sa):
     """In-mask FLOPs per step: total and the band kernel's share (non-global rows)."""
     per_head, total = sa.count_pairs(w.N, w.window, w.dilation, w.H, w.globals_)
@@ -364,7 +372,10 @@ def run_ours(args):
                        "pct_of_bf16_peak": 100.0 * value / (world * pk["bf16_tflops"])},
             "roofline": {"bound": "tensor", "kernel": "band", "achieved": band_tflops,
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": band_tflops / pk["bf16_tflops"], "traffic": None,
+                         "frac": band_tflops / pk["bf16_tflops"],
+                         "traffic": (BAND_DRAM_BYTES_PER_HEAD * w.B * w.H if args.workload == 5
+                                     else None),
+                         "traffic_source": "ncu DRAM bytes of a 2-head launch, scaled by heads",
                          "peak_source": f"{pk['source']} bf16 dense (burst)",
                          "frac_of_sustained": (band_tflops / pk["bf16_tflops_sustained"]
                                                if pk.get("bf16_tflops_sustained") else None),
