@@ -57,7 +57,20 @@ typedef enum {
   SA_ERR_NO_MEMORY = 5    /* device scratch could not be allocated           */
 } sa_status;
 
-typedef enum { SA_BF16 = 0, SA_FP32 = 1 } sa_dtype;
+/*
+ * Input / output element type and the precision of the products:
+ *  SA_BF16  bf16 in memory; bf16 x bf16 products on the tensor cores, fp32
+ *           accumulation and softmax, bf16 output.
+ *  SA_FP32  fp32 in memory; fp32 arithmetic throughout on the CUDA cores,
+ *           fp32 output.
+ *  SA_TF32  fp32 in memory; the two products on the tensor cores in tf32 (the
+ *           inputs' lowest 13 mantissa bits do not take part), fp32
+ *           accumulation, softmax and output.  D = 64 only.  For scales near
+ *           1/sqrt(D) the error is a fraction of bf16's; a scale several
+ *           times larger sharpens the softmax until tf32 scores no longer meet
+ *           fp32 accuracy -- use SA_FP32 there.
+ */
+typedef enum { SA_BF16 = 0, SA_FP32 = 1, SA_TF32 = 2 } sa_dtype;
 
 /* Largest number of distinct global positions accepted. */
 #define SA_MAX_GLOBALS 256
@@ -73,8 +86,8 @@ typedef enum { SA_BF16 = 0, SA_FP32 = 1 } sa_dtype;
  *  global_idx host, n_global entries in [0, N); duplicates are merged (a set).
  *            May be NULL when n_global == 0.  At most SA_MAX_GLOBALS distinct.
  *  scale     multiplier of q.k before the softmax (finite).
- *  dtype     SA_BF16 (tensor-core path, fp32 accumulation and softmax, bf16
- *            output) or SA_FP32 (fp32 arithmetic throughout, fp32 output).
+ *  dtype     SA_BF16, SA_FP32 or SA_TF32 (see sa_dtype; SA_TF32 with D other
+ *            than 64 is SA_ERR_UNSUPPORTED).
  *  stream    cudaStream_t on which all work is enqueued.
  *
  * Device scratch (gathered global rows, split-K partials) comes from a
@@ -238,8 +251,8 @@ sa_status sa_profile_end(sa_profile *out);
  * cudaFree or other allocating routine.
  *
  *  Arguments, layouts, ownership and validation are those of sa_forward_lse
- *  (lse may be NULL).  The arithmetic runs on the CUDA cores in fp32 for both
- *  input types (bf16 in and out for SA_BF16), so results agree with
+ *  (lse may be NULL).  The arithmetic runs on the CUDA cores in fp32 for every
+ *  input type (bf16 in and out for SA_BF16; SA_TF32 runs as SA_FP32), so results agree with
  *  sa_forward_lse within the library's stated tolerance, not bit for bit.
  *
  *  Size limit: a problem whose scratch does not fit the array even after the

@@ -248,7 +248,11 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   sa_status st = device_state(dev, &ds);
   if (st != SA_OK) return st;
 
-  const bool tc = (dtype == SA_BF16);
+  // bf16 -> tensor cores (kind::f16); tf32 (fp32 in memory, D = 64) -> tensor
+  // cores (kind::tf32, no cast of the inputs); fp32 -> CUDA cores, fp32 throughout
+  if (dtype == SA_TF32 && !tc_supports(dtype, D))
+    return fail(SA_ERR_UNSUPPORTED, "SA_TF32 supports D = 64 (got %d)", D);
+  const bool tc = tc_supports(dtype, D);
   const Tiling tiling = tc ? tc_tiling(D) : kSimtTiling;
   const DeviceSchedule *sched = nullptr;
   st = get_schedule(*ds, p, tc ? 1 : 0, tiling, &sched);
@@ -300,6 +304,19 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
     off_po = carve(part_rows * D * sizeof(float));
     off_ml = carve(part_rows * 2 * sizeof(float));
   }
+  // fp32 on the tensor cores: transposed values (per slot, the global-row
+  // pass's, the gathered globals')
+  const bool tf32 = dtype == SA_TF32;
+  size_t off_vts = 0, off_vtp = 0, off_vtg = 0;
+  if (tf32) {
+    size_t per_slot = 0;
+    for (const Slot &sl : hs.slots) per_slot += (size_t)BH * D * values_len_pad(sl.len) * 4;
+    off_vts = carve(per_slot);
+    if (dp.n_g > 0) {
+      off_vtp = carve((size_t)BH * D * values_len_pad(N) * 4);
+      off_vtg = carve((size_t)BH * D * hs.g_pad * 4);
+    }
+  }
   char *scratch = nullptr;
   if (total > 0) {
     e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&scratch), total, ds->pool, stream);
@@ -310,6 +327,13 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
     dp.vg = scratch + off_v;
     dp.part_o = reinterpret_cast<float *>(scratch + off_po);
     dp.part_ml = reinterpret_cast<float *>(scratch + off_ml);
+    if (tf32) {
+      dp.vT_slots = reinterpret_cast<float *>(scratch + off_vts);
+      if (dp.n_g > 0) {
+        dp.vT_plain = reinterpret_cast<float *>(scratch + off_vtp);
+        dp.vgT = reinterpret_cast<float *>(scratch + off_vtg);
+      }
+    }
   }
 
   sa_status result = SA_OK;
@@ -321,14 +345,32 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
     if (le != cudaSuccess) result = cuda_fail(le, what);
   };
   if (dp.n_g > 0) step(0, [&] { return launch_gather(dp, BH, dtype, stream); }, "gather launch");
+  if (tf32) {
+    step(0, [&] {
+      size_t off = 0;
+      for (const Slot &sl : hs.slots) {
+        const int lp = values_len_pad(sl.len);
+        cudaError_t le = launch_transpose_values(static_cast<const float *>(v), dp.vT_slots + off, N,
+                                                 D, sl.r, sl.d, sl.len, lp, BH, stream);
+        if (le != cudaSuccess) return le;
+        off += (size_t)BH * D * lp;
+      }
+      if (dp.n_g == 0) return cudaSuccess;
+      cudaError_t le = launch_transpose_values(static_cast<const float *>(dp.gv_src), dp.vT_plain, N,
+                                               D, 0, 1, N, values_len_pad(N), BH, stream);
+      if (le != cudaSuccess) return le;
+      return launch_transpose_values(static_cast<const float *>(dp.vg), dp.vgT, hs.g_pad, D, 0, 1,
+                                     hs.g_pad, hs.g_pad, BH, stream);
+    }, "value transposition launch");
+  }
   if (tc)
-    step(1, [&] { return launch_band_tc(dp, hs.slots.data(), (int)hs.slots.size(), hs.group_begin, BH, stream); },
+    step(1, [&] { return launch_band_tc(dp, dtype, hs.slots.data(), (int)hs.slots.size(), hs.group_begin, BH, stream); },
          "band (tensor-core) launch");
   else
     step(1, [&] { return launch_band_simt(dp, dtype, stream); }, "band launch");
   if (dp.n_g > 0) {
     if (tc)
-      step(2, [&] { return launch_global_tc(dp, BH, stream); }, "global-row (tensor-core) launch");
+      step(2, [&] { return launch_global_tc(dp, dtype, BH, stream); }, "global-row (tensor-core) launch");
     else
       step(2, [&] { return launch_global_simt(dp, dtype, stream); }, "global-row launch");
     step(3, [&] { return launch_merge(dp, BH, dtype, stream); }, "merge launch");

@@ -37,6 +37,11 @@ struct DevProblem {
   int n_chunks, chunk_len;
   // scratch
   void *qg, *kg, *vg;  // [B*H][g_pad][D] gathered global rows, input dtype
+  // fp32 inputs on the tensor cores (tf32): values transposed so that the P V
+  // product reads them K-major (tf32 operands must be K-major)
+  float *vT_slots;  // per residue-class slot s, back to back: [B*H][D][len_pad(s)]
+  float *vT_plain;  // [B*H][D][round_up(N, 4)] of the global-row pass's values
+  float *vgT;       // [B*H][D][g_pad] of the gathered global values
   float *part_o;       // [B*H][n_chunks][g_pad][D]  unnormalised partial outputs
   float *part_ml;      // [B*H][n_chunks][g_pad][2]  partial (max, sum), base 2
   int *err;
@@ -60,5 +65,10 @@ cudaError_t launch_gather(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t
 cudaError_t launch_band_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s);
 cudaError_t launch_global_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s);
 cudaError_t launch_merge(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s);
+// dst[bh][d][t] = src[bh][r + step t][d] for t < len, 0 for len <= t < len_pad
+// (src: [BH][n_src][D] fp32); len_pad a multiple of 4.
+cudaError_t launch_transpose_values(const float *src, float *dst, int n_src, int D, int r,
+                                    int step, int len, int len_pad, int BH, cudaStream_t s);
+inline int values_len_pad(int len) { return (len + 3) & ~3; }
 
 }  // namespace sa

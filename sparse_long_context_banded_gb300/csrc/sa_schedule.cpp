@@ -47,7 +47,7 @@ std::string validate(const Problem &p) {
     for (int h = 0; h < p.H; ++h)
       if (p.dilation[h] != 1) return "the chunked pattern takes no dilation";
   }
-  if (p.dtype != SA_BF16 && p.dtype != SA_FP32) return "unknown dtype";
+  if (p.dtype != SA_BF16 && p.dtype != SA_FP32 && p.dtype != SA_TF32) return "unknown dtype";
   const double elems = (double)p.B * p.H * p.N * std::max(p.D, 1);
   if (elems > 9.0e18) return "tensor too large";
   return "";

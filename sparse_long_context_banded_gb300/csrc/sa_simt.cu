@@ -310,6 +310,33 @@ cudaError_t global_simt_launch(const DevProblem &p, cudaStream_t s) {
 
 }  // namespace
 
+// 32 x 32 tiles through shared memory: coalesced reads of value rows,
+// coalesced writes of the transposed rows.
+__global__ void transpose_values_kernel(const float *src, float *dst, int n_src, int D, int r,
+                                        int step, int len, int len_pad) {
+  __shared__ float tile[32][33];
+  const int t0 = blockIdx.x * 32, d0 = blockIdx.y * 32, bh = blockIdx.z;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int i = ty; i < 32; i += 8) {
+    const int t = t0 + i;
+    tile[i][tx] = (t < len && d0 + tx < D)
+                      ? src[((int64_t)bh * n_src + r + (int64_t)step * t) * D + d0 + tx]
+                      : 0.f;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int d = d0 + i, t = t0 + tx;
+    if (d < D && t < len_pad) dst[((int64_t)bh * D + d) * len_pad + t] = tile[tx][i];
+  }
+}
+
+cudaError_t launch_transpose_values(const float *src, float *dst, int n_src, int D, int r,
+                                    int step, int len, int len_pad, int BH, cudaStream_t s) {
+  dim3 grid((len_pad + 31) / 32, (D + 31) / 32, BH), block(32, 8);
+  transpose_values_kernel<<<grid, block, 0, s>>>(src, dst, n_src, D, r, step, len, len_pad);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s) {
   dim3 grid(p.g_pad, BH);
   if (dt == SA_BF16)

@@ -65,10 +65,6 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
 constexpr int kFarAway = -(1 << 30);  // class coordinate of a global outside the class
 constexpr bool kGlobalsFirst = false;  // global key tiles before (or after) the band tiles
-// Output tiles: staged in the tile's query buffer and written by TMA (the
-// buffer is released by the epilogue), or written from registers (the buffer
-// is released by the tile's last S MMA).
-constexpr bool kStagedStore = true;
 
 struct Maps {
   CUtensorMap q[kMaxSlotsPerLaunch], k[kMaxSlotsPerLaunch], v[kMaxSlotsPerLaunch],
@@ -86,12 +82,15 @@ struct Params {
   int n_items;      // work items of this launch (CTAs stride over them)
 };
 
-template <int D>
+// TF: fp32 inputs on the tensor cores as tf32 (kind::tf32), else bf16 (kind::f16).
+template <int D, bool TF>
 struct Cfg {
-  static constexpr int kQBytes = kRows * D * 2;    // one query tile
-  static constexpr int kSlotBytes = kKeys * D * 2; // one key or value tile
-  static constexpr int kHalfCols = 64;             // bf16 columns per 128-byte row
-  static constexpr int kHalves = D / 64;
+  static constexpr int kElem = TF ? 4 : 2;             // bytes per input element
+  static constexpr int kQBytes = kRows * D * kElem;    // one query tile
+  static constexpr int kSlotBytes = kKeys * D * kElem; // one key or value tile
+  static constexpr int kHalfCols = 128 / kElem;        // elements per 128-byte row
+  static constexpr int kHalves = D / kHalfCols;
+  static constexpr int kMmaK = 32 / kElem;             // K of one MMA (32 bytes of a row)
   static constexpr int kAux = 3072;  // barriers, flags, global positions (class coordinates)
   static constexpr int kSmemMax = 232448;
   static constexpr int kQBufs = 3;   // query tiles rotate through three buffers
@@ -243,56 +242,60 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // Issue forms for a converged warp: elect.sync picks one lane, which issues the
 // tcgen05 operation (a converged warp with warp-uniform operands issues MMAs at
 // about twice the rate of a single diverged lane).
+template <bool TF>
 __device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p, e;\n"
-      ".reg .b32 r;\n"
-      "elect.sync r|e, 0xffffffff;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (TF)
+    asm volatile(
+        "{\n"
+        ".reg .pred p, e;\n"
+        ".reg .b32 r;\n"
+        "elect.sync r|e, 0xffffffff;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n"
+        ".reg .pred p, e;\n"
+        ".reg .b32 r;\n"
+        "elect.sync r|e, 0xffffffff;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
+template <bool TF>
 __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p, e;\n"
-      ".reg .b32 r;\n"
-      "elect.sync r|e, 0xffffffff;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (TF)
+    asm volatile(
+        "{\n"
+        ".reg .pred p, e;\n"
+        ".reg .b32 r;\n"
+        "elect.sync r|e, 0xffffffff;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n"
+        ".reg .pred p, e;\n"
+        ".reg .b32 r;\n"
+        "elect.sync r|e, 0xffffffff;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
   asm volatile(
@@ -349,10 +352,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
-// Instruction descriptor: bf16 x bf16 -> fp32, M x N, A K-major, B K- or MN-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor: bf16 x bf16 (kind::f16, type 1) or tf32 x tf32
+// (kind::tf32, type 2) -> fp32, M x N, A K-major, B K- or MN-major.
+__host__ __device__ constexpr uint32_t idesc_mma(int M, int N, bool b_mn_major, bool tf32) {
+  return (1u << 4) | ((tf32 ? 2u : 1u) << 7) | ((tf32 ? 2u : 1u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------------------
@@ -510,11 +514,12 @@ __device__ __forceinline__ void load_scores(uint32_t t_s, bool interval, int c_l
 // updated, O in TMEM rescaled when the reference maximum moves.  The reference
 // maximum is raised only when the tile maximum exceeds it by more than 2^8, so
 // O is rescaled rarely; the same reference is used for P and for the running
-// sum, so the result is exact either way.  P is written in two halves of 64
-// keys and the first is announced on bar_half, so that the first half of P V
+// sum, so the result is exact either way.  P (bf16 pairs, or fp32 for fp32
+// inputs) is written over S in two halves of 64 keys and the first is announced
+// on bar_half, so that the first half of P V
 // can start while the second half of P is computed; a global tile has 64 keys
 // (`narrow`) and only its first half is computed.
-template <int D>
+template <int D, bool TF>
 __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float scale, bool interval,
                                              int c_lo, int c_hi, const int32_t *globals, int g0,
                                              int t_q, int half, bool dedup, bool narrow,
@@ -562,16 +567,26 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     if (hh == 1 && narrow) break;
-    uint32_t pr[W / 4];
+    // bf16 P: two keys per TMEM column; tf32 P (fp32 inputs): one
+    constexpr int kWords = TF ? W / 2 : W / 4;
+    uint32_t pr[kWords];
 #pragma unroll
     for (int j = 0; j < W / 4; ++j) {
       const int i = hh * (W / 4) + j;
       const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
       const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
       sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
-      pr[j] = pack_bf16(e.x, e.y);
+      if constexpr (TF) {
+        pr[2 * j] = __float_as_uint(e.x);
+        pr[2 * j + 1] = __float_as_uint(e.y);
+      } else {
+        pr[j] = pack_bf16(e.x, e.y);
+      }
     }
-    tmem_st32(t_s + hh * 32, pr);
+    if constexpr (TF)
+      tmem_st64(t_s + hh * kWords, pr);
+    else
+      tmem_st32(t_s + hh * kWords, pr);
     if (hh == 0) {
       tmem_wait_st();
       tc_fence_before();
@@ -585,9 +600,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
   m_run = m_new;
 }
 
-template <int D, bool GLOBAL>
+template <int D, bool GLOBAL, bool TF>
 __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_constant__ Params P) {
-  using C = Cfg<D>;
+  using C = Cfg<D, TF>;
   constexpr int NS = C::kSlots;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw;
@@ -669,7 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           const CUtensorMap *mq = map_q_of<GLOBAL>(P, wn);
           for (int u = 0; u < 2; ++u)
             if (wn.active[u])
-              for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(mq, 64 * h, q_row_of<GLOBAL>(wn, u), wn.bh);
+              for (int h = 0; h < C::kHalves; ++h)
+                tma_prefetch_3d(mq, C::kHalfCols * h, q_row_of<GLOBAL>(wn, u), wn.bh);
         }
         const CUtensorMap *mq = map_q_of<GLOBAL>(P, w);
         for (int u = 0; u < 2 && ok; ++u) {
@@ -681,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           }
           mbar_expect_tx(B.q_full + 8 * b, C::kQBytes);
           for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(s_q0 + b * C::kQBytes + h * (kRows * 128), mq, B.q_full + 8 * b, 64 * h,
+            tma_load_3d(s_q0 + b * C::kQBytes + h * (kRows * 128), mq, B.q_full + 8 * b, C::kHalfCols * h,
                         q_row_of<GLOBAL>(w, u), w.bh);
           ++j;
         }
@@ -717,10 +733,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
               break;
             }
             const uint32_t dst = s_slots + s * C::kSlotBytes;
-            mbar_expect_tx(B.slot_full + 8 * s, rows * D * 2);
-            for (int h = 0; h < C::kHalves; ++h)
-              tma_load_3d(dst + h * (rows * 128), which ? mv : mk, B.slot_full + 8 * s, 64 * h, y,
-                          w.bh);
+            mbar_expect_tx(B.slot_full + 8 * s, rows * D * C::kElem);
+            if (TF && which) {
+              // transposed values: chunks of 32 keys x D rows (K-major for P V)
+              for (int c = 0; c < rows / 32; ++c)
+                tma_load_3d(dst + c * (D * 128), mv, B.slot_full + 8 * s, y + 32 * c, 0, w.bh);
+            } else {
+              for (int h = 0; h < C::kHalves; ++h)
+                tma_load_3d(dst + h * (rows * 128), which ? mv : mk, B.slot_full + 8 * s,
+                            C::kHalfCols * h, y, w.bh);
+            }
           }
         }
       }
@@ -750,12 +772,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     {
       // a negative scale negates Q in the S products (bit 13: negate A)
       const uint32_t neg_a = p.scale_log2 < 0.f ? (1u << 13) : 0u;
-      const uint32_t kIdescS = idesc_bf16(kRows, kKeys, false) | neg_a;
-      const uint32_t kIdescSg = idesc_bf16(kRows, kGKeys, false) | neg_a;
-      constexpr uint32_t kIdescPV = idesc_bf16(kRows, D, true);
+      const uint32_t kIdescS = idesc_mma(kRows, kKeys, false, TF) | neg_a;
+      const uint32_t kIdescSg = idesc_mma(kRows, kGKeys, false, TF) | neg_a;
+      // B = V: MN-major bf16 tiles as loaded, or K-major transposed fp32 tiles
+      // (tf32 operands must be K-major)
+      constexpr uint32_t kIdescPV = idesc_mma(kRows, D, !TF, TF);
+      // P V: K steps of C::kMmaK keys.  P in TMEM is bf16 pairs (16 keys in 8
+      // columns) or tf32 (8 keys in 8 columns): either way a step advances 8
+      // TMEM columns, and C::kMmaK 128-byte rows of V
+      constexpr int kPvHalf = kKeys / 2 / C::kMmaK;  // steps per half of a band tile
+      constexpr uint64_t kVStep = (uint64_t)C::kMmaK * 128 / 16;
+      // descriptor offset (16-byte units) of P V step kk in a value tile
+      auto v_step = [](int kk) -> uint64_t {
+        if constexpr (TF)
+          return (uint64_t)(((kk >> 2) * (D * 128) + (kk & 3) * 32) >> 4);  // 32-key chunks
+        else
+          return (uint64_t)kk * kVStep;
+      };
       const uint64_t dk_base = sw128_desc(s_slots, 16, 1024);
-      const uint64_t dv_band = sw128_desc(s_slots, kKeys * 128, 1024);   // LBO: next 64 columns of V
-      const uint64_t dv_glob = sw128_desc(s_slots, kGKeys * 128, 1024);
+      const uint64_t dv_band = TF ? sw128_desc(s_slots, 16, 1024)                // K-major
+                                  : sw128_desc(s_slots, kKeys * 128, 1024);  // LBO: next 64 columns of V
+      const uint64_t dv_glob = TF ? sw128_desc(s_slots, 16, 1024) : sw128_desc(s_slots, kGKeys * 128, 1024);
       const uint32_t d_s = tmem + u * 128, d_o = tmem + 256 + u * 128;
       const uint32_t s_full = B.s_full + 8 * u, p_full = B.p_full + 8 * u;
       uint32_t pv = 0, jq = 0, g = 0;  // jq: query tiles of earlier items
@@ -812,20 +849,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
               const uint32_t first = pv_item == 0 ? 0u : 1u;
               if (!gp) {
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 32; ++kk)
-                  mma_ts_warp(d_o, d_s + kk * 8, dv_band + off + (uint64_t)(kk * 128), kIdescPV,
-                              kk > 0 ? 1u : first);
+                for (int kk = 0; kk < kPvHalf; ++kk)
+                  mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_band + off + v_step(kk), kIdescPV,
+                                  kk > 0 ? 1u : first);
                 ok = __all_sync(0xffffffffu, wait_bar(p_full, pv & 1u, abort_flag, p.err));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = kKeys / 32; kk < kKeys / 16; ++kk)
-                  mma_ts_warp(d_o, d_s + kk * 8, dv_band + off + (uint64_t)(kk * 128), kIdescPV, 1u);
+                for (int kk = kPvHalf; kk < 2 * kPvHalf; ++kk)
+                  mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_band + off + v_step(kk), kIdescPV, 1u);
               } else {
 #pragma unroll
-                for (int kk = 0; kk < kGKeys / 16; ++kk)
-                  mma_ts_warp(d_o, d_s + kk * 8, dv_glob + off + (uint64_t)(kk * 128), kIdescPV,
-                              kk > 0 ? 1u : first);
+                for (int kk = 0; kk < kGKeys / C::kMmaK; ++kk)
+                  mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_glob + off + v_step(kk), kIdescPV,
+                                  kk > 0 ? 1u : first);
               }
               ++pv;
               ++pv_item;
@@ -843,19 +880,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
             if (s_reads) {
               tc_fence_after();
               const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
+              // K steps of 32 bytes of a row: four per 128-byte swizzled row
+              // chunk, then on to the next chunk of the tile
               if (!gc) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                  mma_ss_warp(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
-                              dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
+                for (int kk = 0; kk < D / C::kMmaK; ++kk)
+                  mma_ss_warp<TF>(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                                  dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
               } else {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                  mma_ss_warp(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
-                              dk + (((kk >> 2) * (kGKeys * 128) + (kk & 3) * 32) >> 4), kIdescSg, kk > 0);
+                for (int kk = 0; kk < D / C::kMmaK; ++kk)
+                  mma_ss_warp<TF>(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                                  dk + (((kk >> 2) * (kGKeys * 128) + (kk & 3) * 32) >> 4), kIdescSg, kk > 0);
               }
               mma_commit_warp(s_full);
-              if (!kStagedStore && i == last) mma_commit_warp(B.q_empty + 8 * qb);  // Q buffer free
               mma_commit_warp(B.slot_empty + 8 * k_slot);
             } else {
               mbar_arrive_warp(B.slot_empty + 8 * k_slot);
@@ -949,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           g0 = global_index(w, pos) * kGKeys;
           c_hi = min(p.n_g - 1 - g0, kGKeys - 1);
         }
-        softmax_tile<D>(t_s, t_o, sl, interval, c_lo, c_hi, g_list, g0, t_q, half,
+        softmax_tile<D, TF>(t_s, t_o, sl, interval, c_lo, c_hi, g_list, g0, t_q, half,
                         gt && ((w.flags >> u) & 1), gt, B.p_half + 8 * u, lane, m_run, l_run);
         tmem_wait_st();
         tc_fence_before();
@@ -965,18 +1003,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
       ok = fin;
       if (!fin) break;
       tc_fence_after();
-      if (!GLOBAL && !kStagedStore) {
-        // normalise and write this thread's row straight from registers
+      if (!GLOBAL) {
+        // normalise, stage the tile (bf16, or fp32 for fp32 inputs) in this
+        // tile's query buffer (its last S MMA has completed) in the TMA
+        // 128-byte-swizzle layout, and store it with TMA; the buffer is handed
+        // back to the Q producer once the store has read it
+        uint8_t *stage = smem + qb * C::kQBytes;
         const float inv = rcp_approx(l_run);
-        const bool valid = t_q < w.len;
-        const int64_t pos_q = (int64_t)w.r + (int64_t)w.d * t_q;
-        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
-                                                ((int64_t)w.bh * p.N + pos_q) * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32(t_o + c * 32, r);  // collective: every lane loads
-          if (valid) {
+          tmem_ld32(t_o + c * 32, r);
+          // 32 output columns: a quarter of a 128-byte row chunk in bf16, a
+          // whole one in fp32
+          const int h = (c * 32) / C::kHalfCols;
+          const int chunk0 = ((c * 32) % C::kHalfCols) * C::kElem / 16;  // first 16-byte chunk
+          uint8_t *rowp = stage + h * (kRows * 128) + row * 128;
+          if constexpr (TF) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 v = make_float4(
+                  __uint_as_float(r[q4 * 4 + 0]) * inv, __uint_as_float(r[q4 * 4 + 1]) * inv,
+                  __uint_as_float(r[q4 * 4 + 2]) * inv, __uint_as_float(r[q4 * 4 + 3]) * inv);
+              const int phys = (chunk0 + q4) ^ (row & 7);
+              *reinterpret_cast<float4 *>(rowp + phys * 16) = v;
+            }
+          } else {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint4 v;
@@ -984,35 +1036,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
               v.y = pack_bf16(__uint_as_float(r[q4 * 8 + 2]) * inv, __uint_as_float(r[q4 * 8 + 3]) * inv);
               v.z = pack_bf16(__uint_as_float(r[q4 * 8 + 4]) * inv, __uint_as_float(r[q4 * 8 + 5]) * inv);
               v.w = pack_bf16(__uint_as_float(r[q4 * 8 + 6]) * inv, __uint_as_float(r[q4 * 8 + 7]) * inv);
-              orow[c * 4 + q4] = v;
+              const int phys = (chunk0 + q4) ^ (row & 7);
+              *reinterpret_cast<uint4 *>(rowp + phys * 16) = v;
             }
-          }
-        }
-        if (p.lse && valid)
-          p.lse[(int64_t)w.bh * p.N + pos_q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
-      } else if (!GLOBAL) {
-        // normalise, stage the bf16 tile in this tile's query buffer (its last
-        // S MMA has completed) in the TMA 128-byte-swizzle layout, and store it
-        // with TMA; the buffer is handed back to the Q producer once the store
-        // has read it
-        uint8_t *stage = smem + qb * C::kQBytes;
-        const float inv = rcp_approx(l_run);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c * 32, r);
-          const int h = (c * 32) / 64;
-          const int chunk0 = ((c * 32) % 64) / 8;  // first 16-byte chunk in the row
-          uint8_t *rowp = stage + h * (kRows * 128) + row * 128;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(r[q4 * 8 + 0]) * inv, __uint_as_float(r[q4 * 8 + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(r[q4 * 8 + 2]) * inv, __uint_as_float(r[q4 * 8 + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(r[q4 * 8 + 4]) * inv, __uint_as_float(r[q4 * 8 + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(r[q4 * 8 + 6]) * inv, __uint_as_float(r[q4 * 8 + 7]) * inv);
-            const int phys = (chunk0 + q4) ^ (row & 7);
-            *reinterpret_cast<uint4 *>(rowp + phys * 16) = v;
           }
         }
         if (p.lse && t_q < w.len) {
@@ -1024,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
         if (row == 0) {
           const int ls = w.slot - P.slot_base;
           for (int h = 0; h < C::kHalves; ++h)
-            tma_store_3d(&P.maps.o[ls], smem_u32(stage) + h * (kRows * 128), 64 * h,
+            tma_store_3d(&P.maps.o[ls], smem_u32(stage) + h * (kRows * 128), C::kHalfCols * h,
                          (w.q_tile + u) * kRows, w.bh);  // rows past the class end are clipped
           tma_store_commit_and_wait_read();
           mbar_arrive(B.q_empty + 8 * qb);
@@ -1048,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           p.part_ml[slot * 2 + 0] = m_run;
           p.part_ml[slot * 2 + 1] = l_run;
         }
-        if (kStagedStore && row == 0) mbar_arrive(B.q_empty + 8 * qb);  // every S MMA has completed
+        if (row == 0) mbar_arrive(B.q_empty + 8 * qb);  // every S MMA has completed
       }
       // O_u has been read out (tcgen05.ld waits): the next item's first PV_u,
       // issued only after this warpgroup's next P arrival, may overwrite it
@@ -1082,14 +1108,32 @@ cudaError_t get_encoder() {
   return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-// 3-D bf16 map {D, rows, bh}, 128-byte swizzle, boxes of {64, box_rows, 1}.
+// 3-D map {D, rows, bh} of bf16 (or fp32 when tf32), 128-byte swizzle, boxes
+// of {one 128-byte row chunk, box_rows, 1}.
 cudaError_t make_map(CUtensorMap *m, const void *base, int D, uint64_t rows, uint64_t bh,
-                     uint64_t row_stride_bytes, uint64_t bh_stride_bytes, uint32_t box_rows) {
+                     uint64_t row_stride_bytes, uint64_t bh_stride_bytes, uint32_t box_rows,
+                     bool tf32) {
   cuuint64_t dims[3] = {(cuuint64_t)D, rows, bh};
   cuuint64_t strides[2] = {row_stride_bytes, bh_stride_bytes};
-  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t box[3] = {tf32 ? 32u : 64u, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+  CUresult r = g_encode(m, tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        3, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// 3-D fp32 map of transposed values {len_pad (keys), D, bh}, 128-byte swizzle,
+// boxes of {32 keys, D, 1}: one box is the K-major operand chunk of 32 keys.
+cudaError_t make_map_values_t(CUtensorMap *m, const float *base, int D, uint64_t len_pad,
+                              uint64_t bh) {
+  cuuint64_t dims[3] = {len_pad, (cuuint64_t)D, bh};
+  cuuint64_t strides[2] = {len_pad * 4, (cuuint64_t)D * len_pad * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)D, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1098,20 +1142,20 @@ cudaError_t make_map(CUtensorMap *m, const void *base, int D, uint64_t rows, uin
 
 // Persistent launch: one CTA per SM (at most one work item each), every CTA
 // striding over the launch's n_items work items.
-template <int D, bool GLOBAL>
+template <int D, bool GLOBAL, bool TF>
 cudaError_t launch(Params &P, int n_items, cudaStream_t s) {
   if (n_items <= 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  constexpr int smem = Cfg<D>::kSmemBytes;
-  e = cudaFuncSetAttribute(tc_attention_kernel<D, GLOBAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem);
+  constexpr int smem = Cfg<D, TF>::kSmemBytes;
+  e = cudaFuncSetAttribute(tc_attention_kernel<D, GLOBAL, TF>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   P.n_items = n_items;
   const int grid = std::min(n_items, std::max(sms, 1));
-  tc_attention_kernel<D, GLOBAL><<<grid, kThreads, smem, s>>>(P);
+  tc_attention_kernel<D, GLOBAL, TF><<<grid, kThreads, smem, s>>>(P);
   return cudaGetLastError();
 }
 
@@ -1121,72 +1165,94 @@ Tiling tc_tiling(int) { return Tiling{tc::kRows, 2, tc::kKeys, 128, 256, 2 * 152
 
 namespace {
 
-cudaError_t fill_common(tc::Params &P, const DevProblem &p, int BH) {
+cudaError_t fill_common(tc::Params &P, const DevProblem &p, int BH, bool tf) {
   cudaError_t e = tc::get_encoder();
   if (e != cudaSuccess) return e;
   std::memset(&P.maps, 0, sizeof P.maps);
   P.p = p;
   P.p.half = std::min(p.half, p.N);  // a wider window changes nothing
   const int D = p.D;
-  const uint64_t head = (uint64_t)p.N * D * 2;
+  const uint64_t es = tf ? 4 : 2;
+  const uint64_t head = (uint64_t)p.N * D * es;
   if (p.n_g > 0) {
-    const uint64_t ghead = (uint64_t)p.g_pad * D * 2;
-    if ((e = tc::make_map(&P.maps.kg, p.kg, D, p.g_pad, BH, D * 2, ghead, tc::kGKeys)) ||
-        (e = tc::make_map(&P.maps.vg, p.vg, D, p.g_pad, BH, D * 2, ghead, tc::kGKeys)) ||
-        (e = tc::make_map(&P.maps.qg, p.qg, D, p.g_pad, BH, D * 2, ghead, tc::kRows)))
+    const uint64_t ghead = (uint64_t)p.g_pad * D * es;
+    if ((e = tc::make_map(&P.maps.kg, p.kg, D, p.g_pad, BH, D * es, ghead, tc::kGKeys, tf)) ||
+        (e = tf ? tc::make_map_values_t(&P.maps.vg, p.vgT, D, p.g_pad, BH)
+                : tc::make_map(&P.maps.vg, p.vg, D, p.g_pad, BH, D * es, ghead, tc::kGKeys, tf)) ||
+        (e = tc::make_map(&P.maps.qg, p.qg, D, p.g_pad, BH, D * es, ghead, tc::kRows, tf)))
+      return e;
+    // keys and values of the global-row pass
+    if ((e = tc::make_map(&P.maps.kp, p.gk_src, D, p.N, BH, D * es, head, tc::kKeys, tf)) ||
+        (e = tf ? tc::make_map_values_t(&P.maps.vp, p.vT_plain, D, values_len_pad(p.N), BH)
+                : tc::make_map(&P.maps.vp, p.gv_src, D, p.N, BH, D * es, head, tc::kKeys, tf)))
       return e;
   }
-  // keys and values of the global-row pass
-  if ((e = tc::make_map(&P.maps.kp, p.gk_src, D, p.N, BH, D * 2, head, tc::kKeys)) ||
-      (e = tc::make_map(&P.maps.vp, p.gv_src, D, p.N, BH, D * 2, head, tc::kKeys)))
-    return e;
   return cudaSuccess;
+}
+
+template <bool GLOBAL>
+cudaError_t launch_any(tc::Params &P, int D, bool tf, int n_items, cudaStream_t s) {
+  if (tf) return tc::launch<64, GLOBAL, true>(P, n_items, s);  // fp32 inputs: D = 64 only
+  return D == 64 ? tc::launch<64, GLOBAL, false>(P, n_items, s)
+                 : tc::launch<128, GLOBAL, false>(P, n_items, s);
 }
 
 }  // namespace
 
-cudaError_t launch_band_tc(const DevProblem &p, const Slot *host_slots, int n_slots,
+bool tc_supports(sa_dtype dt, int D) {
+  return dt == SA_BF16 ? (D == 64 || D == 128) : dt == SA_TF32 && D == 64;
+}
+
+cudaError_t launch_band_tc(const DevProblem &p, sa_dtype dt, const Slot *host_slots, int n_slots,
                            const std::vector<int32_t> &group_begin, int BH, cudaStream_t s) {
   static thread_local tc::Params P;  // ~9 KB of tensor maps: keep it off the stack
-  cudaError_t e = fill_common(P, p, BH);
+  const bool tf = dt == SA_TF32;
+  cudaError_t e = fill_common(P, p, BH, tf);
   if (e != cudaSuccess) return e;
   const int D = p.D;
-  const uint64_t head = (uint64_t)p.N * D * 2;
+  const uint64_t es = tf ? 4 : 2;
+  const uint64_t head = (uint64_t)p.N * D * es;
+  // transposed values of each slot (tf32), back to back in slot order
+  std::vector<size_t> vt_off(n_slots + 1, 0);
+  for (int i = 0; i < n_slots; ++i)
+    vt_off[i + 1] = vt_off[i] + (size_t)BH * D * values_len_pad(host_slots[i].len);
   const int n_groups = (int)group_begin.size() - 1;
   for (int g = 0; g < n_groups; ++g) {
     const int first = g * tc::kMaxSlotsPerLaunch;
     const int count = std::min(tc::kMaxSlotsPerLaunch, n_slots - first);
     for (int i = 0; i < count; ++i) {
       const Slot &sl = host_slots[first + i];
-      const uint64_t off = (uint64_t)sl.r * D * 2;
-      const uint64_t stride = (uint64_t)sl.d * D * 2;
+      const uint64_t off = (uint64_t)sl.r * D * es;
+      const uint64_t stride = (uint64_t)sl.d * D * es;
       const char *q = static_cast<const char *>(p.q) + off;
       const char *k = static_cast<const char *>(p.k) + off;
       const char *v = static_cast<const char *>(p.v) + off;
       char *o = static_cast<char *>(p.out) + off;
-      if ((e = tc::make_map(&P.maps.q[i], q, D, sl.len, BH, stride, head, tc::kRows)) ||
-          (e = tc::make_map(&P.maps.k[i], k, D, sl.len, BH, stride, head, tc::kKeys)) ||
-          (e = tc::make_map(&P.maps.v[i], v, D, sl.len, BH, stride, head, tc::kKeys)) ||
-          (e = tc::make_map(&P.maps.o[i], o, D, sl.len, BH, stride, head, tc::kRows)))
+      if ((e = tc::make_map(&P.maps.q[i], q, D, sl.len, BH, stride, head, tc::kRows, tf)) ||
+          (e = tc::make_map(&P.maps.k[i], k, D, sl.len, BH, stride, head, tc::kKeys, tf)) ||
+          (e = tf ? tc::make_map_values_t(&P.maps.v[i], p.vT_slots + vt_off[first + i], D,
+                                          values_len_pad(sl.len), BH)
+                  : tc::make_map(&P.maps.v[i], v, D, sl.len, BH, stride, head, tc::kKeys, tf)) ||
+          (e = tc::make_map(&P.maps.o[i], o, D, sl.len, BH, stride, head, tc::kRows, tf)))
         return e;
     }
     P.slot_base = first;
     P.item_offset = group_begin[g];
     const int grid = group_begin[g + 1] - group_begin[g];
-    e = D == 64 ? tc::launch<64, false>(P, grid, s) : tc::launch<128, false>(P, grid, s);
+    e = launch_any<false>(P, D, tf, grid, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
-cudaError_t launch_global_tc(const DevProblem &p, int BH, cudaStream_t s) {
+cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, int BH, cudaStream_t s) {
   static thread_local tc::Params P;
-  cudaError_t e = fill_common(P, p, BH);
+  const bool tf = dt == SA_TF32;
+  cudaError_t e = fill_common(P, p, BH, tf);
   if (e != cudaSuccess) return e;
   P.slot_base = 0;
   P.item_offset = 0;
-  return p.D == 64 ? tc::launch<64, true>(P, p.n_gitems, s)
-                   : tc::launch<128, true>(P, p.n_gitems, s);
+  return launch_any<true>(P, p.D, tf, p.n_gitems, s);
 }
 
 }  // namespace sa

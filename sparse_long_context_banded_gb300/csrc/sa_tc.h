@@ -1,4 +1,6 @@
-// sa_tc.h -- tensor-core (tcgen05 / TMEM / TMA) kernels for bf16 inputs.
+// sa_tc.h -- tensor-core (tcgen05 / TMEM / TMA) kernels: bf16 inputs
+// (kind::f16, D 64 or 128) and fp32 inputs with tf32 products (SA_TF32:
+// kind::tf32, D 64).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -11,12 +13,15 @@ namespace sa {
 
 Tiling tc_tiling(int D);
 
+// Whether the tensor-core kernels take inputs of this type and head dimension.
+bool tc_supports(sa_dtype dt, int D);
+
 // Band tiles: one launch per group of at most 16 residue classes
 // (group_begin from the schedule).  host_slots mirrors p.slots on the host.
-cudaError_t launch_band_tc(const DevProblem &p, const Slot *host_slots, int n_slots,
+cudaError_t launch_band_tc(const DevProblem &p, sa_dtype dt, const Slot *host_slots, int n_slots,
                            const std::vector<int32_t> &group_begin, int BH, cudaStream_t s);
 
 // Global rows against all keys, split over key chunks (partials for merge).
-cudaError_t launch_global_tc(const DevProblem &p, int BH, cudaStream_t s);
+cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, int BH, cudaStream_t s);
 
 }  // namespace sa

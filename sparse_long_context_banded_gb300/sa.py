@@ -17,7 +17,7 @@ import numpy as np
 from . import build as _build
 
 SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_TIMEOUT, SA_ERR_NO_MEMORY = range(6)
-SA_BF16, SA_FP32 = 0, 1
+SA_BF16, SA_FP32, SA_TF32 = 0, 1, 2
 SA_MAX_GLOBALS = 256
 STAGES = ("gather", "band", "global_rows", "merge")
 
@@ -112,10 +112,12 @@ def count_pairs(N: int, window: int, dilation: Sequence[int] | None, H: int,
 
 def forward(q, k, v, window: int, dilation: Sequence[int] | None = None,
             globals_: Sequence[int] = (), scale: Optional[float] = None, out=None,
-            lse=None, stream=None):
+            lse=None, stream=None, tf32: bool = False):
     """out = sparse attention of torch CUDA tensors q, k, v ([B, H, N, D]).
 
     ``lse``: None, or a float32 CUDA tensor [B, H, N] to receive log-sum-exp.
+    ``tf32``: for float32 tensors, run the products on the tensor cores in tf32
+    (SA_TF32, D = 64) instead of fp32 on the CUDA cores (SA_FP32).
     Runs on ``stream`` (default: torch's current stream); returns ``out``.
     """
     import torch
@@ -123,7 +125,7 @@ def forward(q, k, v, window: int, dilation: Sequence[int] | None = None,
     if q.dtype == torch.bfloat16:
         dt = SA_BF16
     elif q.dtype == torch.float32:
-        dt = SA_FP32
+        dt = SA_TF32 if tf32 else SA_FP32
     else:
         raise TypeError(f"unsupported dtype {q.dtype} (bfloat16 or float32)")
     for t in (q, k, v):

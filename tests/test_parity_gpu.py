@@ -25,12 +25,12 @@ def to_device(a, torch):
     return torch.from_numpy(a).cuda()
 
 
-def run_gpu(q, k, v, window, dilation, globals_, scale=None):
+def run_gpu(q, k, v, window, dilation, globals_, scale=None, tf32=False):
     import torch
     tq, tk, tv = (to_device(a, torch) for a in (q, k, v))
     B, H, N, D = q.shape
     lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
-    out = sa.forward(tq, tk, tv, window, dilation, globals_, scale=scale, lse=lse)
+    out = sa.forward(tq, tk, tv, window, dilation, globals_, scale=scale, lse=lse, tf32=tf32)
     sa.sync_status()
     return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
@@ -114,6 +114,39 @@ def test_scale_sign_and_size(case, oracle):
     assert_lse_close(got_lse, ref_lse, str(case))
 
 
+# fp32 inputs with tf32 products on the tensor cores (SA_TF32, D = 64): the
+# fp32 cases above at the workloads' scale 1/sqrt(D), every row.
+TF32_CASES = [
+    (1, 2, 1024, 64, 512, [1, 1], [0]),               # the tiny Longformer-mask shape
+    (1, 2, 777, 64, 300, [1, 2], [5, 700, 5]),
+    (2, 1, 129, 64, 0, [1], []),
+    (1, 1, 1, 64, 16, [1], [0]),
+    (1, 3, 640, 64, 128, [1, 2, 3], [639]),
+    (1, 1, 200, 64, 0, [1], list(range(200))),        # every position global
+    (1, 2, 300, 64, 1000, [1, 1], []),                # dense
+    (1, 1, 2050, 64, 600, [4], list(range(0, 2050, 97))),
+]
+
+
+@pytest.mark.parametrize("case", TF32_CASES, ids=lambda c: "B{}H{}N{}w{}d{}g{}".format(
+    c[0], c[1], c[2], c[4], max(c[5]), len(c[6])))
+def test_tf32_full(case, oracle):
+    B, H, N, D, window, dil, G = case
+    q, k, v = make(B, H, N, D, "fp32", seed=zlib.crc32(repr(case).encode()))
+    got, got_lse = run_gpu(q, k, v, window, dil, G, tf32=True)
+    ref, ref_lse = oracle.forward_longformer(q, k, v, window, dil, G)
+    assert_close(got, ref, "tf32 " + str(case))
+    assert_lse_close(got_lse, ref_lse, "tf32 " + str(case))
+
+
+def test_tf32_rejects_d128():
+    import torch
+    q = torch.zeros((1, 1, 64, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(sa.SaError) as e:
+        sa.forward(q, q, q, 16, tf32=True)
+    assert e.value.status == sa.SA_ERR_UNSUPPORTED
+
+
 def sample_rows(w, rng, n_random):
     """Flattened row ids covering tile seams, the tail, globals and random rows."""
     rows = set()
@@ -141,6 +174,17 @@ def workload_inputs(number):
         w = inputs.workload(number)
         _cache[number] = (w, inputs.draw_qkv(w))
     return _cache[number]
+
+
+def test_tiny_workload_tf32(oracle):
+    """The fp32 tiny Longformer-mask workload through the tf32 tensor-core path,
+    every row."""
+    w, (q, k, v) = workload_inputs(1)
+    got, got_lse = run_gpu(q, k, v, w.window, w.dilation, w.globals_, w.scale, tf32=True)
+    ref, ref_lse = oracle.forward_longformer(q, k, v, w.window, w.dilation, w.globals_,
+                                             scale=w.scale)
+    assert_close(got, ref, "tf32 " + w.describe())
+    assert_lse_close(got_lse, ref_lse, "tf32 " + w.describe())
 
 
 @pytest.mark.parametrize("number", [1, 2, 3, 4, 5])
