@@ -189,11 +189,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
-// Commit the issued bulk stores and wait until they have read shared memory.
-__device__ __forceinline__ void tma_store_commit_and_wait_read() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -670,13 +665,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
   if (warp == 8 && lane == 1) {
     // ------------------------------------------------------------- Q producer
     // Query tiles are loaded in order (item by item, tile 0 then tile 1) into
-    // the buffers 0, 1, 2, 0, ...; a buffer is refilled once the output tile
-    // staged in it has been stored, so the next item's first query tile lands
-    // in the spare buffer while the current item is still running.  The following item's query rows are
-    // prefetched into L2.
+    // the buffers 0, 1, 2, 0, ...; the next item's first query tile lands in
+    // the spare buffer while the current item is still running, and the
+    // following item's query rows are prefetched into L2.  The softmax
+    // warpgroup stages each finished output tile in its query buffer; this
+    // thread stores it with TMA when the buffer comes round again (or at the
+    // end), so that no softmax warp waits for a store to read shared memory.
     {
       uint32_t j = 0;  // query tiles loaded so far
       bool ok = true;
+      // output tile staged in each buffer: map index, first row, head
+      int out_ls[NQ], out_row[NQ], out_bh[NQ];
+      auto store_staged = [&](uint32_t b) {
+        for (int h = 0; h < C::kHalves; ++h)
+          tma_store_3d(&P.maps.o[out_ls[b]], s_q0 + b * C::kQBytes + h * (kRows * 128),
+                       C::kHalfCols * h, out_row[b], out_bh[b]);  // rows past the class end are clipped
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      };
       for (int item = item0; item < n_items && ok; item += stride) {
         const Work w = make_work<GLOBAL>(P, item);
         if (item + stride < n_items) {
@@ -695,6 +700,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
             ok = false;
             break;
           }
+          if (!GLOBAL && use > 0) {
+            // the previous occupant's output tile is staged: store it, and
+            // reload the buffer once the store has read it
+            store_staged(b);
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          }
+          if (!GLOBAL) {
+            out_ls[b] = w.slot - P.slot_base;
+            out_row[b] = (w.q_tile + u) * kRows;
+            out_bh[b] = w.bh;
+          }
           mbar_expect_tx(B.q_full + 8 * b, C::kQBytes);
           for (int h = 0; h < C::kHalves; ++h)
             tma_load_3d(s_q0 + b * C::kQBytes + h * (kRows * 128), mq, B.q_full + 8 * b, C::kHalfCols * h,
@@ -706,7 +722,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
         // the last loads may still be in flight: let them land
         for (uint32_t x = j > (uint32_t)NQ ? j - NQ : 0u; x < j; ++x)
           wait_bar(B.q_full + 8 * (x % NQ), (x / NQ) & 1u, abort_flag, nullptr, false);
+      } else if (!GLOBAL) {
+        // the last output tiles: store each once it is staged
+        for (uint32_t x = j > (uint32_t)NQ ? j - NQ : 0u; x < j; ++x) {
+          if (!wait_bar(B.q_empty + 8 * (x % NQ), (x / NQ) & 1u, abort_flag, p.err)) break;
+          store_staged(x % NQ);
+        }
       }
+      // every store issued has finished reading shared memory and writing
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------- K/V producer
@@ -1045,16 +1069,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           const int64_t pos_q = (int64_t)w.r + (int64_t)w.d * t_q;
           p.lse[(int64_t)w.bh * p.N + pos_q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
         }
+        // the staged tile is handed to the Q producer, which stores it
         fence_proxy_async_smem();
         named_bar_sync(bar_id, 128);
-        if (row == 0) {
-          const int ls = w.slot - P.slot_base;
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_store_3d(&P.maps.o[ls], smem_u32(stage) + h * (kRows * 128), C::kHalfCols * h,
-                         (w.q_tile + u) * kRows, w.bh);  // rows past the class end are clipped
-          tma_store_commit_and_wait_read();
-          mbar_arrive(B.q_empty + 8 * qb);
-        }
+        if (row == 0) mbar_arrive(B.q_empty + 8 * qb);
       } else {
         const int gr = q_row_of<GLOBAL>(w, u) + row;
         const int64_t slot = ((int64_t)w.bh * p.n_chunks + w.chunk) * p.g_pad + gr;
