@@ -206,6 +206,18 @@ sa_status sa_forward_gather(const void *q, const void *k, const void *v, const i
                             void *out, float *lse, int B, int H, int Nq, int Nk, int D, int K,
                             float scale, sa_dtype dtype, sa_stream_t stream);
 
+/*
+ * sa_check_stalled_wait -- exercises the failure detection of the kernels
+ * without a GPU fault: enqueues on `stream` one small kernel that waits on a
+ * barrier nothing will ever arrive on, through the same bounded wait the
+ * attention kernels use, but giving up after `limit_us` microseconds (1 ..
+ * 2,000,000) instead of two seconds.  It then sets the device error word and
+ * returns, leaving the context usable: the next sa_sync_status(stream) returns
+ * SA_ERR_TIMEOUT (and clears the word).  SA_ERR_INVALID_ARG for a limit out of
+ * range; SA_ERR_CUDA if the launch fails.
+ */
+sa_status sa_check_stalled_wait(uint32_t limit_us, sa_stream_t stream);
+
 /* Thread-local description of the last non-OK status on this host thread. */
 const char *sa_last_error(void);
 

@@ -529,6 +529,23 @@ extern "C" sa_status sa_count_pairs(int N, int window, const int32_t *dilation, 
 
 extern "C" const char *sa_last_error(void) { return t_last_error.c_str(); }
 
+extern "C" sa_status sa_check_stalled_wait(uint32_t limit_us, sa_stream_t stream) {
+  if (limit_us < 1 || limit_us > 2000000)
+    return fail(SA_ERR_INVALID_ARG, "limit_us must be in [1, 2000000] (got %u)", limit_us);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState *ds = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    sa_status st = device_state(dev, &ds);
+    if (st != SA_OK) return st;
+  }
+  e = launch_stalled_wait_check(ds->err, limit_us, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stalled-wait check launch");
+  return SA_OK;
+}
+
 extern "C" sa_status sa_sync_status(sa_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

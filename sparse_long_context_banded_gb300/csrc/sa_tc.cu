@@ -1263,6 +1263,33 @@ cudaError_t launch_band_tc(const DevProblem &p, sa_dtype dt, const Slot *host_sl
   return cudaSuccess;
 }
 
+namespace {
+// Failure-detection check: one warp waits on an mbarrier that nothing arrives
+// on, through the same bounded wait the attention kernels use but with a
+// short limit, then records the timeout in the error word and returns.
+__global__ void stalled_wait_kernel(int *err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = tc::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    tc::mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  const uint64_t start = tc::global_timer();
+  while (!tc::mbar_try_wait(b, 0)) {
+    if (tc::global_timer() - start > limit_ns) {
+      if (threadIdx.x == 0) atomicOr(err, kErrWaitTimeout);
+      break;
+    }
+  }
+}
+}  // namespace
+
+cudaError_t launch_stalled_wait_check(int *err, uint32_t limit_us, cudaStream_t s) {
+  stalled_wait_kernel<<<1, 32, 0, s>>>(err, (uint64_t)limit_us * 1000ull);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, int BH, cudaStream_t s) {
   static thread_local tc::Params P;
   const bool tf = dt == SA_TF32;

@@ -21,6 +21,10 @@ bool tc_supports(sa_dtype dt, int D);
 cudaError_t launch_band_tc(const DevProblem &p, sa_dtype dt, const Slot *host_slots, int n_slots,
                            const std::vector<int32_t> &group_begin, int BH, cudaStream_t s);
 
+// Failure-detection check: a kernel whose wait can never be satisfied gives
+// up after limit_us microseconds and sets kErrWaitTimeout in *err.
+cudaError_t launch_stalled_wait_check(int *err, uint32_t limit_us, cudaStream_t s);
+
 // Global rows against all keys, split over key chunks (partials for merge).
 cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, int BH, cudaStream_t s);
 

@@ -39,6 +39,7 @@ SIGNATURES = {
     "sa_count_pairs": (_I, [_I, _I, _I32P, _I, _I32P, _I, _I64P, _I64P]),
     "sa_last_error": (ctypes.c_char_p, []),
     "sa_sync_status": (_I, [_VP]),
+    "sa_check_stalled_wait": (_I, [ctypes.c_uint32, _VP]),
     "sa_profile_begin": (_I, []),
     "sa_profile_end": (_I, [ctypes.POINTER(_Profile)]),
     "sa_version": (ctypes.c_char_p, []),
@@ -297,6 +298,15 @@ def sync_status(stream=None):
     import torch
     s = stream or torch.cuda.current_stream()
     _check(load().sa_sync_status(ctypes.c_void_p(s.cuda_stream)))
+
+
+def check_stalled_wait(limit_us: int = 20000, stream=None):
+    """Enqueue the failure-detection check (sa_check_stalled_wait): a kernel
+    whose wait is never satisfied gives up after ``limit_us`` microseconds; the
+    next ``sync_status`` raises SaError(SA_ERR_TIMEOUT)."""
+    import torch
+    s = stream or torch.cuda.current_stream()
+    _check(load().sa_check_stalled_wait(int(limit_us), ctypes.c_void_p(s.cuda_stream)))
 
 
 def profile_begin():
