@@ -340,37 +340,64 @@ def run_ours(args):
     band_tflops = band_flops / (band_ms * 1e-3) / 1e12
     launches = sum(p["launches"] for p in prof.values())
 
-    # end to end through the public call: pinned host inputs in, result back to host
+    # end to end through the public call: every step copies its inputs in from
+    # pinned host memory and its result back out.  Steps are pipelined over two
+    # device buffer sets and three streams (inputs of step i+1 copied in, and
+    # the result of step i-1 copied out, while step i computes), as a serving
+    # loop would run them.
     e2e = None
     if not args.no_e2e:
         pq, pk_, pv = (t.pin_memory() for t in (hq, hk, hv))
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        for _ in range(2):
-            q.copy_(pq, non_blocking=True)
-            k.copy_(pk_, non_blocking=True)
-            v.copy_(pv, non_blocking=True)
-            step()
-            hout.copy_(out, non_blocking=True)
+        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        bufs = [(q, k, v, out), tuple(torch.empty_like(x) for x in (q, k, v, out))]
+        s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in", "cmp", "out")}
+
+        def e2e_steps_run(n):
+            for i in range(n):
+                b = i % 2
+                dq, dk, dv, dout = bufs[b]
+                if i >= 2:
+                    s_in.wait_event(ev["cmp"][b])   # step i-2 has read this input set
+                with torch.cuda.stream(s_in):
+                    dq.copy_(pq, non_blocking=True)
+                    dk.copy_(pk_, non_blocking=True)
+                    dv.copy_(pv, non_blocking=True)
+                ev["in"][b].record(s_in)
+                s_cmp.wait_event(ev["in"][b])
+                if i >= 2:
+                    s_cmp.wait_event(ev["out"][b])  # step i-2's result has been copied out
+                sa.forward(dq, dk, dv, w.window, w.dilation, w.globals_, scale=w.scale, out=dout,
+                           stream=s_cmp, tf32=tf32)
+                ev["cmp"][b].record(s_cmp)
+                s_out.wait_event(ev["cmp"][b])
+                with torch.cuda.stream(s_out):
+                    hout[b].copy_(dout, non_blocking=True)
+                ev["out"][b].record(s_out)
+
+        e2e_steps_run(2)
         torch.cuda.synchronize()
-        e2e_steps = max(3, min(args.steps, 10))
+        e2e_steps = max(4, min(args.steps, 12))
         barrier(world)
         torch.cuda.synchronize()
         x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        x0.record(stream)
-        for _ in range(e2e_steps):
-            q.copy_(pq, non_blocking=True)
-            k.copy_(pk_, non_blocking=True)
-            v.copy_(pv, non_blocking=True)
-            step()
-            hout.copy_(out, non_blocking=True)
-        x1.record(stream)
+        x0.record(s_in)
+        s_cmp.wait_event(x0)
+        s_out.wait_event(x0)
+        e2e_steps_run(e2e_steps)
+        s_out.wait_stream(s_in)
+        s_out.wait_stream(s_cmp)
+        x1.record(s_out)
         torch.cuda.synchronize()
+        sa.sync_status(s_cmp)
         ms_e2e = max_over_ranks(x0.elapsed_time(x1), world, dev)
         h2d = 3 * q.numel() * q.element_size()
         d2h = out.numel() * out.element_size()
         e2e = {"value": world * flops_step * e2e_steps / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": ms_e2e / e2e_steps, "steps": e2e_steps}
+               "ms_per_step": ms_e2e / e2e_steps, "steps": e2e_steps,
+               "pipelined": "step i+1's inputs copied in and step i-1's result copied out "
+                            "while step i computes (two buffer sets, three streams)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
