@@ -147,6 +147,38 @@ def test_tf32_rejects_d128():
     assert e.value.status == sa.SA_ERR_UNSUPPORTED
 
 
+# The largest global set (SA_MAX_GLOBALS = 256): four 64-key global tiles per
+# band item and two 128-row query tiles per global-row item, with and without
+# dilation, scattered and contiguous.
+MAX_GLOBAL_CASES = [
+    (1, 2, 3000, 128, 256, [1, 2], "scattered", "bf16"),
+    (1, 1, 2049, 64, 512, [1], "prefix", "bf16"),
+    (1, 1, 1500, 64, 100, [3], "scattered", "fp32"),
+]
+
+
+@pytest.mark.parametrize("case", MAX_GLOBAL_CASES, ids=lambda c: "N{}D{}d{}{}{}".format(
+    c[2], c[3], max(c[5]), c[6], c[7]))
+def test_max_globals(case, oracle):
+    B, H, N, D, window, dil, kind, dtype = case
+    rng = np.random.default_rng(N)
+    G = (sorted(rng.choice(N, sa.SA_MAX_GLOBALS, replace=False).tolist()) if kind == "scattered"
+         else list(range(sa.SA_MAX_GLOBALS)))
+    q, k, v = make(B, H, N, D, dtype, seed=zlib.crc32(repr(case).encode()))
+    got, got_lse = run_gpu(q, k, v, window, dil, G)
+    ref, ref_lse = oracle.forward_longformer(q, k, v, window, dil, G)
+    assert_close(got, ref, str(case))
+    assert_lse_close(got_lse, ref_lse, str(case))
+
+
+def test_too_many_globals_rejected():
+    import torch
+    q = torch.zeros((1, 1, 300, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sa.SaError) as e:
+        sa.forward(q, q, q, 16, None, list(range(sa.SA_MAX_GLOBALS + 1)))
+    assert e.value.status == sa.SA_ERR_UNSUPPORTED
+
+
 def sample_rows(w, rng, n_random):
     """Flattened row ids covering tile seams, the tail, globals and random rows."""
     rows = set()
