@@ -3,8 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 5] [--impl ours|reference]
 
 One step = one sa_forward call over one batch of the long-context workload
-(B=1, H=16, N=131072, D=128, window 1024, globals 0..63, bf16): gather of the
-global rows, band tiles, global-row split-K pass, merge.  The metric is useful
+(B=1, H=16, N=131072, D=128, window 1024, globals 0..63, bf16): band tiles,
+global-row split-K pass, merge (the global rows are contiguous, so they are read
+in place; a scattered set adds a gather).  The metric is useful
 (in-mask) attention FLOP/s: 4*D per scored (query, key) pair, pairs counted
 exactly by sa_count_pairs.  Inputs (1.6 GB) are larger than the 129 MB L2, so
 no flush is needed between steps.

@@ -278,6 +278,12 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   dp.globals = sched->globals;
   dp.n_g = (int)p.globals.size();
   dp.g_pad = hs.g_pad;
+  // contiguous globals (a first token, a memory prefix): the tensor-core kernels
+  // read them through views of the inputs, and nothing is gathered
+  dp.g_first = -1;
+  if (tc && !p.globals.empty() &&
+      p.globals.back() - p.globals.front() + 1 == (int32_t)p.globals.size())
+    dp.g_first = p.globals.front();
   dp.slots = sched->slots;
   dp.band = sched->band;
   dp.n_band = (int)hs.band.size();
@@ -344,7 +350,8 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
     timer.done();
     if (le != cudaSuccess) result = cuda_fail(le, what);
   };
-  if (dp.n_g > 0) step(0, [&] { return launch_gather(dp, BH, dtype, stream); }, "gather launch");
+  if (dp.n_g > 0 && dp.g_first < 0)
+    step(0, [&] { return launch_gather(dp, BH, dtype, stream); }, "gather launch");
   if (tf32) {
     step(0, [&] {
       size_t off = 0;
@@ -359,6 +366,9 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
       cudaError_t le = launch_transpose_values(static_cast<const float *>(dp.gv_src), dp.vT_plain, N,
                                                D, 0, 1, N, values_len_pad(N), BH, stream);
       if (le != cudaSuccess) return le;
+      if (dp.g_first >= 0)  // straight from the contiguous rows of v
+        return launch_transpose_values(static_cast<const float *>(v), dp.vgT, N, D, dp.g_first, 1,
+                                       std::min(hs.g_pad, N - dp.g_first), hs.g_pad, BH, stream);
       return launch_transpose_values(static_cast<const float *>(dp.vg), dp.vgT, hs.g_pad, D, 0, 1,
                                      hs.g_pad, hs.g_pad, BH, stream);
     }, "value transposition launch");

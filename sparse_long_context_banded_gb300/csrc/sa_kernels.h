@@ -29,6 +29,10 @@ struct DevProblem {
   float scale_log2; // scale * log2(e): scores are kept in base-2 units
   const int32_t *globals;  // device, sorted unique, n_g entries
   int n_g, g_pad;
+  // >= 0: the globals are the contiguous positions [g_first, g_first + n_g), and
+  // the tensor-core kernels read their rows through views of q (or the global
+  // queries' source), k and v instead of gathered copies; -1 otherwise
+  int g_first;
   const Slot *slots;
   const BandItem *band;
   int n_band;

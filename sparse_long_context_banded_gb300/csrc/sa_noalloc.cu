@@ -189,6 +189,7 @@ extern "C" sa_status sa_forward_noalloc(const void *q, const void *k, const void
   dp.gq_src = q;
   dp.gk_src = k;
   dp.gv_src = v;
+  dp.g_first = -1;  // the CUDA-core kernels read gathered rows
   dp.out = out;
   dp.lse = lse;
   dp.N = N;

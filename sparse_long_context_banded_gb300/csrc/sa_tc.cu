@@ -1192,13 +1192,27 @@ cudaError_t fill_common(tc::Params &P, const DevProblem &p, int BH, bool tf) {
   const int D = p.D;
   const uint64_t es = tf ? 4 : 2;
   const uint64_t head = (uint64_t)p.N * D * es;
-  if (p.n_g > 0) {
+  if (p.n_g > 0 && p.g_first >= 0) {
+    // contiguous globals: views of the rows [g_first, N) of the inputs (rows past
+    // the globals are read but masked; rows past N read as zeros)
+    const uint64_t off = (uint64_t)p.g_first * D * es, rows = (uint64_t)(p.N - p.g_first);
+    const char *kv = static_cast<const char *>(p.k) + off;
+    const char *vv = static_cast<const char *>(p.v) + off;
+    const char *qv = static_cast<const char *>(p.gq_src) + off;
+    if ((e = tc::make_map(&P.maps.kg, kv, D, rows, BH, D * es, head, tc::kGKeys, tf)) ||
+        (e = tf ? tc::make_map_values_t(&P.maps.vg, p.vgT, D, p.g_pad, BH)
+                : tc::make_map(&P.maps.vg, vv, D, rows, BH, D * es, head, tc::kGKeys, tf)) ||
+        (e = tc::make_map(&P.maps.qg, qv, D, rows, BH, D * es, head, tc::kRows, tf)))
+      return e;
+  } else if (p.n_g > 0) {
     const uint64_t ghead = (uint64_t)p.g_pad * D * es;
     if ((e = tc::make_map(&P.maps.kg, p.kg, D, p.g_pad, BH, D * es, ghead, tc::kGKeys, tf)) ||
         (e = tf ? tc::make_map_values_t(&P.maps.vg, p.vgT, D, p.g_pad, BH)
                 : tc::make_map(&P.maps.vg, p.vg, D, p.g_pad, BH, D * es, ghead, tc::kGKeys, tf)) ||
         (e = tc::make_map(&P.maps.qg, p.qg, D, p.g_pad, BH, D * es, ghead, tc::kRows, tf)))
       return e;
+  }
+  if (p.n_g > 0) {
     // keys and values of the global-row pass
     if ((e = tc::make_map(&P.maps.kp, p.gk_src, D, p.N, BH, D * es, head, tc::kKeys, tf)) ||
         (e = tf ? tc::make_map_values_t(&P.maps.vp, p.vT_plain, D, values_len_pad(p.N), BH)

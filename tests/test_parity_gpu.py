@@ -260,12 +260,19 @@ def test_profile_counts_launches():
     import torch
     q, k, v = make(1, 1, 512, 64, "bf16", seed=6)
     tq, tk, tv = (to_device(a, torch) for a in (q, k, v))
+    # scattered globals: gather, band, global rows, merge
     sa.profile_begin()
     for _ in range(3):
-        sa.forward(tq, tk, tv, 64, None, [3])
+        sa.forward(tq, tk, tv, 64, None, [3, 100])
     prof = sa.profile_end()
     assert [prof[s]["launches"] for s in sa.STAGES] == [3, 3, 3, 3]
     assert all(prof[s]["ms"] > 0 for s in sa.STAGES)
+    # contiguous globals: read in place, nothing gathered
+    sa.profile_begin()
+    for _ in range(3):
+        sa.forward(tq, tk, tv, 64, None, [3, 4, 5])
+    prof = sa.profile_end()
+    assert [prof[s]["launches"] for s in sa.STAGES] == [0, 3, 3, 3]
     sa.profile_begin()
     sa.forward(tq, tk, tv, 64, None, [])
     prof = sa.profile_end()
