@@ -262,29 +262,52 @@ __global__ void __launch_bounds__(NT) global_simt_kernel(DevProblem p) {
 // ---------------------------------------------------------------------------
 // merge: m = max_c m_c, l = sum_c l_c 2^(m_c - m), o = sum_c o_c 2^(m_c - m) / l.
 // One block per (global row, head); writes that global row of `out` (and lse).
+// Upper bound of the key chunks of the global-row pass (the schedule asks for
+// at most a few hundred CTAs).
+constexpr int kMaxMergeChunks = 1024;
+
 template <typename T>
 __global__ void merge_kernel(DevProblem p) {
-  const int g = blockIdx.x, bh = blockIdx.y;
+  // One block per (global row, head).  The chunks' (max, sum) pairs are read
+  // once, in parallel, and reduced across the block; each thread then sums its
+  // output columns over the chunks with independent loads.
+  __shared__ float w_chunk[kMaxMergeChunks];
+  __shared__ float red[4];
+  const int g = blockIdx.x, bh = blockIdx.y, t = threadIdx.x;
   const int64_t first = ((int64_t)bh * p.n_chunks) * p.g_pad + g;
   const int64_t step = p.g_pad;
+  const int nc = p.n_chunks;
+  // maximum over the chunks
   float m = -INFINITY;
-  for (int c = 0; c < p.n_chunks; ++c) m = fmaxf(m, p.part_ml[(first + c * step) * 2]);
+  for (int c = t; c < nc; c += blockDim.x) m = fmaxf(m, p.part_ml[(first + c * step) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((t & 31) == 0) red[t >> 5] = m;
+  __syncthreads();
+  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  // chunk weights and the total sum
   float l = 0.f;
-  for (int c = 0; c < p.n_chunks; ++c) {
+  for (int c = t; c < nc; c += blockDim.x) {
     const int64_t s = first + c * step;
-    l += p.part_ml[s * 2 + 1] * exp2f(p.part_ml[s * 2] - m);
+    const float wc = exp2f(p.part_ml[s * 2] - m);
+    w_chunk[c] = wc;
+    l += p.part_ml[s * 2 + 1] * wc;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  if ((t & 31) == 0) red[t >> 5] = l;
+  __syncthreads();
+  l = red[0] + red[1] + red[2] + red[3];
   const float inv = 1.f / l;
   const int64_t orow = ((int64_t)bh * p.N + p.globals[g]) * p.D;
-  for (int d = threadIdx.x; d < p.D; d += blockDim.x) {
+  for (int d = t; d < p.D; d += blockDim.x) {
     float o = 0.f;
-    for (int c = 0; c < p.n_chunks; ++c) {
-      const int64_t s = first + c * step;
-      o += p.part_o[s * p.D + d] * exp2f(p.part_ml[s * 2] - m);
-    }
+#pragma unroll 8
+    for (int c = 0; c < nc; ++c) o += p.part_o[(first + c * step) * p.D + d] * w_chunk[c];
     st<T>(p.out, orow + d, o * inv);
   }
-  if (p.lse && threadIdx.x == 0)
+  if (p.lse && t == 0)
     p.lse[(int64_t)bh * p.N + p.globals[g]] = (m + log2f(l)) * 0.6931471805599453f;
 }
 
@@ -361,6 +384,7 @@ cudaError_t launch_global_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s)
 }
 
 cudaError_t launch_merge(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s) {
+  if (p.n_chunks > kMaxMergeChunks) return cudaErrorInvalidValue;
   dim3 grid(p.n_g, BH);
   if (dt == SA_BF16)
     merge_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(p);
