@@ -1,21 +1,24 @@
-// sa_tc.cu -- tensor-core kernels (sm_103a: TMA, mbarrier, tcgen05 + TMEM)
-// for bf16 inputs: the band-tile kernel and the global-row split-K kernel.
+// sa_tc.cu -- tensor-core kernels (sm_103a: TMA, mbarrier, tcgen05 + TMEM):
+// the band-tile kernel and the global-row split-K kernel, for bf16 inputs
+// (kind::f16) and for fp32 inputs with tf32 products (kind::tf32, D = 64).
 //
 // What one CTA computes (Unlimiformer section 2.3 Eq. (1) under the additive
 // {0,-inf} mask of GMAT's "Global-Memory Augmented Transformers" section):
 // two 128-row query tiles Q_0, Q_1, each against its own list of key tiles --
 // the band tiles that intersect its rows' windows (Longformer glossary, "How
 // the Longformer attention works": sliding / dilated window) followed by the
-// gathered global keys (the same section's global attention; GMAT "Global
-// Memory") -- with an exact online softmax in fp32.  The two query tiles are
-// neighbours, so their band lists overlap and each key/value tile is loaded
-// once for both.
+// global keys (the same section's global attention; GMAT "Global Memory") --
+// with an exact online softmax in fp32.  The two query tiles are neighbours, so
+// their band lists overlap and each key/value tile is loaded once for both.
+// The global rows are read from gathered copies, or in place through views of
+// q, k, v when they are contiguous.
 //
-//   S = Q_u K_j^T (tcgen05, fp32 in TMEM; Q negated for a negative scale) ->
-//   mask (edge tiles only), running max / sum per row -> P = exp2(scale S - m)
-//   as bf16 written back into the same TMEM columns, in two halves -> O_u +=
-//   P V_j (tcgen05, A operand from TMEM; the first half of the product starts
-//   once the first half of P is in place).
+//   S = Q_u K_j^T (fp32 in TMEM; Q negated for a negative scale) -> mask (edge
+//   tiles only), running max / sum per row -> P = exp2(scale S - m) written
+//   back over S (bf16 pairs, or fp32 for tf32), in two halves -> O_u += P V_j
+//   (A operand from TMEM; the first half of the product starts once the first
+//   half of P is in place).  tf32 operands must be K-major, so for fp32 inputs
+//   the values arrive transposed (32-key chunks of D rows).
 //
 // In global mode the two query tiles are the gathered global rows and the key
 // tiles one chunk of all N keys; the CTA writes unnormalised partial outputs
@@ -26,15 +29,15 @@
 // so the next item's Q load and first MMAs overlap the current item's tail.
 //
 // Warp roles (352 threads): warps 0-3 softmax of Q_0 (one thread per row; they
-// also write the finished rows), warps 4-7 softmax of Q_1, warp 8 TMA producers
-// (lane 0 keys/values, lane 1 queries), warp 9 MMA issuer of Q_0 (and TMEM
-// allocator), warp 10 MMA issuer of Q_1.  TMEM: S_0 cols [0,128), S_1 [128,256), O_0
-// [256,256+D), O_1 [384,384+D).  Shared memory: three query-tile buffers
-// (used in rotation, so the next item's first query tile can land while both
-// current ones are in use; a finished output tile is staged in its query
-// tile's buffer), then a ring of key/value slots (one K or V tile each), then
-// barriers.  All tiles use the
-// 128-byte swizzle that TMA writes and the UMMA descriptors read.
+// also normalise and stage the finished rows), warps 4-7 softmax of Q_1, warp 8
+// TMA producers (lane 0 keys/values; lane 1 queries, and the TMA store of each
+// staged output tile), warp 9 MMA issuer of Q_0 (and TMEM allocator), warp 10
+// MMA issuer of Q_1.  TMEM: S_0 cols [0,128), S_1 [128,256), O_0 [256,256+D),
+// O_1 [384,384+D).  Shared memory: three query-tile buffers (used in rotation,
+// so the next item's first query tile can land while both current ones are in
+// use; a finished output tile is staged in its query tile's buffer), then a
+// ring of key/value slots (one K or V tile each), then barriers.  All tiles use
+// the 128-byte swizzle that TMA writes and the UMMA descriptors read.
 //
 // Every wait on an mbarrier is bounded: after kWaitLimitNs the waiting thread
 // sets the CTA's abort flag and the device error word, and every role winds
