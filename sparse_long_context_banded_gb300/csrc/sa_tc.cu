@@ -980,6 +980,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
         }
         named_bar_sync(bar_id, 128);
       }
+      // this row's key interval and the tile's extreme rows (band mode); a
+      // band tile is full when every row's interval covers it -- the intervals
+      // only move forward with the row, so the first row has the earliest end
+      // and the last row the latest start
+      int r_lo = 0, r_hi = 0, lo_last = 0, hi_first = 0;
+      if (!GLOBAL) {
+        const int q0 = (w.q_tile + u) * kRows;
+        int unused;
+        row_keys(half, p.chunk, p.memory, w.len, q0 + kRows - 1, lo_last, unused);
+        row_keys(half, p.chunk, p.memory, w.len, q0, unused, hi_first);
+        row_keys(half, p.chunk, p.memory, w.len, t_q, r_lo, r_hi);
+      }
       float m_run = -INFINITY, l_run = 0.f;
       for (int i = 0; i < n && ok; ++i) {
         const int pos = seq_pos_s(w, nlo_u, ncnt_u, i);
@@ -996,15 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
             interval = kb + kKeys > w.key_end;
             c_hi = w.key_end - 1 - kb;
           } else {
-            // the tile is full when every row's key interval covers it; the
-            // intervals only move forward with the row, so the first row has
-            // the earliest end and the last row the latest start
-            const int q0 = (w.q_tile + u) * kRows;
-            int lo_last, hi_first, r_lo, r_hi, unused;
-            row_keys(half, p.chunk, p.memory, w.len, q0 + kRows - 1, lo_last, unused);
-            row_keys(half, p.chunk, p.memory, w.len, q0, unused, hi_first);
             interval = !(lo_last <= kb && hi_first >= kb + kKeys - 1);
-            row_keys(half, p.chunk, p.memory, w.len, t_q, r_lo, r_hi);
             c_lo = r_lo - kb;
             c_hi = r_hi - kb;
           }
