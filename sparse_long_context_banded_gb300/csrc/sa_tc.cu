@@ -996,10 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
       for (int i = 0; i < n && ok; ++i) {
         const int pos = seq_pos_s(w, nlo_u, ncnt_u, i);
         const bool gt = is_global_pos(w, pos);
-        ok = __all_sync(0xffffffffu, wait_bar(B.s_full + 8 * u, scnt & 1u, abort_flag, p.err));
-        ++scnt;
-        if (!ok) break;
-        tc_fence_after();
+        // the tile's masks are set up before its S is awaited
         bool interval = true;
         int c_lo = 0, c_hi, g0 = 0;
         if (!gt) {
@@ -1018,8 +1015,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           g0 = global_index(w, pos) * kGKeys;
           c_hi = min(p.n_g - 1 - g0, kGKeys - 1);
         }
+        const bool dedup = gt && ((w.flags >> u) & 1);
+        ok = __all_sync(0xffffffffu, wait_bar(B.s_full + 8 * u, scnt & 1u, abort_flag, p.err));
+        ++scnt;
+        if (!ok) break;
+        tc_fence_after();
         softmax_tile<D, TF>(t_s, t_o, sl, interval, c_lo, c_hi, g_list, g0, t_q, half,
-                        gt && ((w.flags >> u) & 1), gt, B.p_half + 8 * u, lane, m_run, l_run);
+                        dedup, gt, B.p_half + 8 * u, lane, m_run, l_run);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
