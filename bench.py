@@ -79,10 +79,10 @@ def peaks():
 
 # DRAM bytes (read + write) of one band-kernel launch per head of the
 # long-context workload: ncu dram__bytes_read.sum + dram__bytes_write.sum of the
-# 2-head capture in profiles/band_kernel_long_context_h2.md (259.9 MB), halved.
+# 2-head capture in profiles/band_kernel_long_context_h2.md (260.1 MB), halved.
 # Heads are independent slices of the same work, so a launch over H heads moves
 # H times this.  Valid for the kernel build that capture was taken of.
-BAND_DRAM_BYTES_PER_HEAD = (216_905_728 + 42_968_320) / 2
+BAND_DRAM_BYTES_PER_HEAD = (217_288_448 + 42_845_440) / 2
 
 
 def workload_flops(w, sa):
