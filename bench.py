@@ -421,7 +421,9 @@ def run_ours(args):
                               if flush is None else
                               f"inputs ({in_bytes / 1e6:.0f} MB) smaller than L2: a 512 MB "
                               f"buffer written between steps, outside the per-step events"),
-                       "pct_of_bf16_peak": 100.0 * value / (world * pk["bf16_tflops"])},
+                       "pct_of_bf16_peak": 100.0 * value / (world * pk["bf16_tflops"]),
+                       "pct_of_bf16_peak_sustained": (100.0 * value / (world * pk["bf16_tflops_sustained"])
+                                                      if pk.get("bf16_tflops_sustained") else None)},
             "roofline": {"bound": "tensor", "kernel": "band", "achieved": band_tflops,
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": band_tflops / pk["bf16_tflops"],
