@@ -73,6 +73,8 @@ SMALL_CASES = [
     (2, 2, 515, 128, 200, [2, 1], [0, 1, 514], "fp32"),
     (1, 2, 4096, 128, 1024, [1, 1], list(range(64)), "bf16"),
     (1, 1, 2050, 64, 600, [4], list(range(0, 2050, 97)), "bf16"),
+    (1, 2, 1500, 64, 255, [1, 2], [3, 1499], "bf16"),    # odd window: half width 127
+    (1, 2, 2000, 128, 511, [1, 3], [7, 100, 1999], "bf16"),
 ]
 
 
