@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     # about a second of timed work at the default workload, so that the 200 ms
     # clock sampler sees the GPU under load several times
-    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--steps", type=int, default=600)  # >= 50: the headline is their median
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="5",
                     help="workload number 1..5, or 'gather' for the list-attention workload")
@@ -77,12 +77,26 @@ def peaks():
             "source": "fallback"}
 
 
-# DRAM bytes (read + write) of one band-kernel launch per head of the
-# long-context workload: ncu dram__bytes_read.sum + dram__bytes_write.sum of the
-# 2-head capture in profiles/band_kernel_long_context_h2.md (260.1 MB), halved.
-# Heads are independent slices of the same work, so a launch over H heads moves
-# H times this.  Valid for the kernel build that capture was taken of.
-BAND_DRAM_BYTES_PER_HEAD = (217_288_448 + 42_845_440) / 2
+def measured_traffic(workload: int):
+    """DRAM bytes (read + write) per launch of the attention kernel from an ncu
+    capture, if one was taken of the kernel source as it is now: the capture's
+    record names the SHA-256 of the kernel source it was taken of, and a record
+    of another source gives None."""
+    import hashlib
+    rec_path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "sparse_long_context_banded_gb300", "csrc", "sa_tc.cu")
+    if not os.path.exists(rec_path):
+        return None, "no ncu capture recorded"
+    with open(rec_path) as f:
+        rec = json.load(f)
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    entry = rec.get(str(workload))
+    if not entry:
+        return None, "no ncu capture of this workload"
+    if entry.get("kernel_source_sha256") != digest:
+        return None, "ncu capture taken of another kernel source"
+    return entry["dram_bytes_per_launch"], entry["source"]
 
 
 def workload_flops(w, sa):
@@ -305,41 +319,58 @@ def run_ours(args):
     # the per-step events, so that no step finds its inputs in L2
     in_bytes = 4 * q.numel() * q.element_size()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if in_bytes < (512 << 20) else None
+    # timed region: K steps with no instrumentation but one CUDA event between
+    # consecutive steps (the per-step times; their median is the headline)
     sampler = ClockSampler(local)
     sampler.start()
     barrier(world)
     torch.cuda.synchronize()
-    sa.profile_begin()
     if flush is None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        evs[0].record(stream)
+        for i in range(args.steps):
             step()
-        e1.record(stream)
+            evs[i + 1].record(stream)
         torch.cuda.synchronize()
-        ms_local = e0.elapsed_time(e1)
+        step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     else:
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for a, b in evs:
+        pairs_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(args.steps)]
+        for a, b in pairs_ev:
             flush.zero_()
             a.record(stream)
             step()
             b.record(stream)
         torch.cuda.synchronize()
-        ms_local = sum(a.elapsed_time(b) for a, b in evs)
-    prof = sa.profile_end()
+        step_ms = [a.elapsed_time(b) for a, b in pairs_ev]
     barrier(world)
     clocks = sampler.stop()
     sa.sync_status(stream)
-    ms_total = max_over_ranks(ms_local, world, dev)
-    ms_step = ms_total / args.steps
-    value = job_value(flops_step, args.steps, ms_total, world)
+    ms_median_local = statistics.median(step_ms)
+    ms_step = max_over_ranks(ms_median_local, world, dev)
+    ms_mean = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    value = job_value(flops_step, 1, ms_step, world)
+
+    # per-kernel times from a separate, instrumented pass (CUDA events around
+    # every launch on the launching stream)
+    prof_steps = max(10, min(50, args.steps))
+    sa.profile_begin()
+    for _ in range(prof_steps):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    prof = sa.profile_end()
+    launches_per_step = sum(p["launches"] for p in prof.values()) / prof_steps
 
     pk = peaks()
-    band_ms = prof["band"]["ms"] / max(1, prof["band"]["launches"])
-    band_tflops = band_flops / (band_ms * 1e-3) / 1e12
-    launches = sum(p["launches"] for p in prof.values())
+    # the dominant kernel: the band launch, which on the tensor cores also runs
+    # the global rows (then its algorithmic work is every in-mask pair)
+    fused = prof["global_rows"]["launches"] == 0 and len(w.globals_) > 0
+    kern_flops = flops_step if fused else band_flops
+    kern_ms = prof["band"]["ms"] / max(1, prof["band"]["launches"])
+    kern_tflops = kern_flops / (kern_ms * 1e-3) / 1e12
+    traffic, traffic_src = measured_traffic(args.workload) if not args.heads else (None, "")
 
     # end to end through the public call: every step copies its inputs in from
     # pinned host memory and its result back out.  Steps are pipelined over two
@@ -411,6 +442,8 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "ms_per_step_stat": f"median of {args.steps} per-step CUDA-event times "
+                                f"(max over ranks); mean {ms_mean:.4f} ms",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
             if w.dtype == "bf16" else ("tf32" if tf32 else "fp32"), "data": "synthetic",
             "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D,
@@ -424,21 +457,23 @@ def run_ours(args):
                        "pct_of_bf16_peak": 100.0 * value / (world * pk["bf16_tflops"]),
                        "pct_of_bf16_peak_sustained": (100.0 * value / (world * pk["bf16_tflops_sustained"])
                                                       if pk.get("bf16_tflops_sustained") else None)},
-            "roofline": {"bound": "tensor", "kernel": "band", "achieved": band_tflops,
+            "roofline": {"bound": "tensor",
+                         "kernel": "band + global rows (one launch)" if fused else "band",
+                         "achieved": kern_tflops,
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": band_tflops / pk["bf16_tflops"],
-                         "traffic": (BAND_DRAM_BYTES_PER_HEAD * w.B * w.H if args.workload == 5
-                                     else None),
-                         "traffic_source": "ncu DRAM bytes of a 2-head launch, scaled by heads",
+                         "frac": kern_tflops / pk["bf16_tflops"],
+                         "traffic": traffic, "traffic_source": traffic_src,
                          "peak_source": f"{pk['source']} bf16 dense (burst)",
-                         "frac_of_sustained": (band_tflops / pk["bf16_tflops_sustained"]
+                         "frac_of_sustained": (kern_tflops / pk["bf16_tflops_sustained"]
                                                if pk.get("bf16_tflops_sustained") else None),
-                         "algorithmic_flops_per_launch": band_flops,
-                         "ms_per_launch": band_ms},
-            "stages_ms_per_step": {s: prof[s]["ms"] / max(1, prof[s]["launches"]) for s in prof},
+                         "algorithmic_flops_per_launch": kern_flops,
+                         "ms_per_launch": kern_ms,
+                         "timing": f"CUDA events around each launch, {prof_steps} steps of a "
+                                   f"separate pass after the timed region"},
+            "stages_ms_per_step": {s: prof[s]["ms"] / prof_steps for s in prof},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches,
+            "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

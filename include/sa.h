@@ -72,6 +72,45 @@ typedef enum {
  */
 typedef enum { SA_BF16 = 0, SA_FP32 = 1, SA_TF32 = 2 } sa_dtype;
 
+/*
+ * Precision of the P V product on the bf16 tensor-core path.  The softmax
+ * weights P are computed in fp32; the tensor cores multiply bf16 operands.
+ *  SA_PV_SINGLE  P is rounded to one bf16 value (8 significant bits).  The
+ *                rounding errors of a row's weights average out over many
+ *                comparable keys; on a row whose softmax rests on a few keys
+ *                they do not, and the output error can exceed the library's
+ *                tolerance |err| <= 2e-3 + 1e-2 |ref| where |ref| is small.
+ *  SA_PV_SPLIT   P = P_hi + P_lo, two bf16 values (16 significant bits); the
+ *                P V product runs over both (1.5x the tensor-core work of
+ *                SA_PV_SINGLE).  The tolerance holds for every row.
+ *  SA_PV_AUTO    (default) SA_PV_SPLIT when some non-global row sees fewer
+ *                than 128 keys (a narrow window, a short chunk) or when
+ *                |scale| sqrt(D) > 1.25 (scores sharper than the usual
+ *                1/sqrt(D) scaling of unit-variance q and k), else
+ *                SA_PV_SINGLE.  The choice looks at shapes and the scale
+ *                only: inputs whose norms make the softmax sharp at the usual
+ *                scale need SA_PV_SPLIT set explicitly.
+ * SA_FP32 and SA_TF32 keep P in fp32 / tf32 and are not affected.
+ */
+typedef enum { SA_PV_AUTO = 0, SA_PV_SINGLE = 1, SA_PV_SPLIT = 2 } sa_pv_mode;
+
+/*
+ * sa_set_pv_mode -- process-wide choice for the calls enqueued after it
+ * returns (an atomic setting; calls already enqueued are not affected).
+ * SA_ERR_INVALID_ARG for an unknown mode.  sa_get_pv_mode returns the setting.
+ */
+sa_status sa_set_pv_mode(sa_pv_mode mode);
+sa_pv_mode sa_get_pv_mode(void);
+
+/*
+ * sa_uses_split_p -- 1 if a bf16 call with these shapes and scale would split
+ * P under the current setting, else 0 (chunk = 0 for the band pattern, else
+ * the chunk length and n_memory of sa_forward_chunked).  Host only.
+ */
+int sa_uses_split_p(int N, int D, int window, const int32_t *dilation, int H,
+                    const int32_t *global_idx, int n_global, int chunk, int n_memory,
+                    float scale);
+
 /* Largest number of distinct global positions accepted. */
 #define SA_MAX_GLOBALS 256
 
@@ -137,6 +176,11 @@ sa_status sa_forward_global_proj(const void *q, const void *k, const void *v,
  * element (*total, may be NULL).  Host only, integer arithmetic, no GPU use.
  * Same arguments and validation as sa_forward.  The in-mask FLOP count of a
  * call is 4 * D * B * total (2D for q.k and 2D for p*v per pair).
+ * This is the count of the mask-count example in the Ultralytics glossary
+ * "Longformer", section "How the Longformer attention works" (window 512,
+ * global token 0): 461,054 / 988,414 / 2,043,134 scored pairs at
+ * N = 1024 / 2048 / 4096, which the section prints rounded as 0.5M / 1.0M /
+ * 2.0M against full attention's N^2.
  */
 sa_status sa_count_pairs(int N, int window, const int32_t *dilation, int H,
                          const int32_t *global_idx, int n_global, int64_t *per_head,
@@ -233,10 +277,12 @@ sa_status sa_sync_status(sa_stream_t stream);
  * sa_forward* call records CUDA events around each of its kernel launches on
  * its own stream.  sa_profile_end() waits for those events and returns, per
  * stage, the number of launches and their summed device time in milliseconds.
- * Stages: 0 gather of global rows, 1 band tiles (or the list attention of
- * sa_forward_gather), 2 global-row split-K pass, 3 merge of partial softmax
- * statistics.  Process-wide; not for concurrent use
- * from several threads.
+ * Stages: 0 gather of global rows, 1 band tiles (with the global-row split-K
+ * work when it runs in the same launch, as on the tensor cores with at most
+ * 16 residue classes; or the list attention of sa_forward_gather),
+ * 2 global-row split-K pass as a launch of its own, 3 merge of partial
+ * softmax statistics.  Process-wide; not for concurrent use from several
+ * threads.  Each launch is also an NVTX range ("sa.band", "sa.merge", ...).
  */
 #define SA_NUM_STAGES 4
 typedef struct {

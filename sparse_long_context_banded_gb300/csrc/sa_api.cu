@@ -1,19 +1,27 @@
 // sa_api.cu -- the C ABI: argument checks, schedule cache, scratch, launches.
 //
 // One sa_forward call enqueues, on the caller's stream:
-//   1. gather    -- q/k/v rows of the global positions into compact buffers
+//   1. gather    -- q/k/v rows of a scattered global set into compact buffers
+//                   (contiguous globals are read in place on the tensor cores)
 //   2. band      -- per query tile: the key tiles of its band, then the global
-//                   key tile(s); writes every row of `out` (global rows too)
-//   3. global    -- the global rows against all N keys, split over key chunks,
-//                   each CTA leaving a partial (max, sum, unnormalised output)
-//   4. merge     -- combines the partials and overwrites the global rows
-// Steps 1, 3 and 4 run only when the global set is not empty.
+//                   key tile(s); writes every row of `out` (global rows too).
+//      global    -- the global rows against all N keys, split over key chunks,
+//                   each CTA leaving partials (max, sum, unnormalised output).
+//                   On the tensor cores both kinds of work run in one launch,
+//                   on CTAs of their own (the global rows' CTAs read K and V
+//                   while the band CTAs compute); on the CUDA cores, and when
+//                   one launch cannot address every residue class, the global
+//                   rows are a launch of their own.
+//   3. merge     -- combines the partials and overwrites the global rows
+// Steps 1 and 3 and the global-row work run only when the global set is not
+// empty.
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <memory>
 #include <mutex>
@@ -24,6 +32,8 @@
 #include "sa_internal.h"
 #include "sa_kernels.h"
 #include "sa_tc.h"
+
+#include <nvtx3/nvToolsExt.h>
 
 namespace sa {
 namespace {
@@ -46,6 +56,14 @@ sa_status cuda_fail(cudaError_t e, const char *what) {
 
 // ---------------------------------------------------------------------------
 // per-device state: error word, scratch pool, cached schedules
+//
+// One mutex guards this state; it is held only while a call looks up or
+// builds its schedule and while it hands the schedule back, never across the
+// launches.  A schedule evicted from the cache is retired: its device buffers
+// are freed once no call is still enqueuing with it and every event recorded
+// after a call that used it has completed (no device-wide synchronisation).  A
+// schedule used by a call under stream capture is never freed, since the
+// captured graph may run it at any later time.
 
 struct DeviceSchedule {
   Schedule host;
@@ -53,12 +71,18 @@ struct DeviceSchedule {
   BandItem *band = nullptr;
   GlobalItem *global = nullptr;
   int32_t *globals = nullptr;
+  int active = 0;                       // calls between lookup and release
+  std::vector<cudaEvent_t> inflight;    // recorded after each call that used it
+  bool captured = false;                // used under stream capture: keep forever
 };
 
 struct DeviceState {
   int *err = nullptr;
   cudaMemPool_t pool = nullptr;
+  int sms = 0;
   std::map<std::string, std::unique_ptr<DeviceSchedule>> schedules;
+  std::vector<std::unique_ptr<DeviceSchedule>> retired;
+  std::vector<cudaEvent_t> spare_events;
 };
 
 std::mutex g_mutex;
@@ -76,6 +100,8 @@ sa_status device_state(int dev, DeviceState **out) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
   e = cudaMemset(ds->err, 0, sizeof(int));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+  e = cudaDeviceGetAttribute(&ds->sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
   cudaMemPoolProps props{};
   props.allocType = cudaMemAllocationTypePinned;
   props.location.type = cudaMemLocationTypeDevice;
@@ -89,22 +115,57 @@ sa_status device_state(int dev, DeviceState **out) {
   return SA_OK;
 }
 
+// Schedule buffers come from the device's stream-ordered pool, so that
+// freeing a retired one never synchronises the device.
 template <typename X>
-sa_status upload(const std::vector<X> &v, X **dst) {
+sa_status upload(const std::vector<X> &v, X **dst, cudaMemPool_t pool, cudaStream_t stream) {
   *dst = nullptr;
   if (v.empty()) return SA_OK;
-  cudaError_t e = cudaMalloc(dst, sizeof(X) * v.size());
-  if (e != cudaSuccess) return fail(SA_ERR_NO_MEMORY, "cudaMalloc(schedule): %s", cudaGetErrorString(e));
-  e = cudaMemcpy(*dst, v.data(), sizeof(X) * v.size(), cudaMemcpyHostToDevice);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(schedule)");
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(dst), sizeof(X) * v.size(), pool,
+                                          stream);
+  if (e != cudaSuccess) {
+    *dst = nullptr;
+    return fail(SA_ERR_NO_MEMORY, "schedule buffer: %s", cudaGetErrorString(e));
+  }
+  e = cudaMemcpyAsync(*dst, v.data(), sizeof(X) * v.size(), cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "copy of the schedule");
   return SA_OK;
 }
 
-void free_schedule(DeviceSchedule &s) {
-  cudaFree(s.slots);
-  cudaFree(s.band);
-  cudaFree(s.global);
-  cudaFree(s.globals);
+void free_schedule(DeviceSchedule &s, cudaStream_t stream) {
+  void *bufs[4] = {s.slots, s.band, s.global, s.globals};
+  for (void *b : bufs)
+    if (b) cudaFreeAsync(b, stream);
+  s.slots = nullptr;
+  s.band = nullptr;
+  s.global = nullptr;
+  s.globals = nullptr;
+}
+
+// Drops the completed events of a schedule (returned to the spare list).
+void prune_events(DeviceState &ds, DeviceSchedule &s) {
+  size_t keep = 0;
+  for (cudaEvent_t ev : s.inflight) {
+    if (cudaEventQuery(ev) == cudaSuccess)
+      ds.spare_events.push_back(ev);
+    else
+      s.inflight[keep++] = ev;
+  }
+  s.inflight.resize(keep);
+}
+
+// Frees the retired schedules that nothing can still read (the frees are
+// enqueued on `stream`, which is not capturing).
+void collect_retired(DeviceState &ds, cudaStream_t stream) {
+  size_t keep = 0;
+  for (auto &r : ds.retired) {
+    prune_events(ds, *r);
+    if (r->active == 0 && r->inflight.empty() && !r->captured)
+      free_schedule(*r, stream);
+    else
+      ds.retired[keep++] = std::move(r);
+  }
+  ds.retired.resize(keep);
 }
 
 std::string schedule_key(const Problem &p, int family) {
@@ -117,43 +178,89 @@ std::string schedule_key(const Problem &p, int family) {
   return k;
 }
 
-// Schedules are immutable once uploaded, so calls on any stream may share them.
-sa_status get_schedule(DeviceState &ds, const Problem &p, int family, const Tiling &t,
-                       const DeviceSchedule **out) {
+// Looks up (or builds and uploads) the schedule and marks it in use; the call
+// hands it back with release_schedule once its work is enqueued.  Schedules
+// are immutable once uploaded, so calls on any stream may share them.  A new
+// schedule is uploaded on `stream` and waited for, so it cannot be built
+// while the stream is capturing.  Called with g_mutex held.
+sa_status acquire_schedule(DeviceState &ds, const Problem &p, int family, const Tiling &t,
+                           cudaStream_t stream, bool capturing, DeviceSchedule **out) {
+  if (!capturing) collect_retired(ds, stream);
   const std::string key = schedule_key(p, family);
   auto it = ds.schedules.find(key);
   if (it != ds.schedules.end()) {
+    it->second->active += 1;
     *out = it->second.get();
     return SA_OK;
   }
+  if (capturing)
+    return fail(SA_ERR_INVALID_ARG, "first call for this problem shape made while the stream is "
+                "capturing: make one call outside capture first (it builds and uploads the "
+                "schedule)");
   if (ds.schedules.size() >= kMaxCachedSchedules) {
-    cudaDeviceSynchronize();  // nothing may still read the evicted schedules
-    for (auto &kv : ds.schedules) free_schedule(*kv.second);
+    for (auto &kv : ds.schedules) ds.retired.push_back(std::move(kv.second));
     ds.schedules.clear();
+    collect_retired(ds, stream);
   }
   auto s = std::make_unique<DeviceSchedule>();
   s->host = build_schedule(p, t);
+  s->host.globals_sorted = p.globals;
   sa_status st;
-  if ((st = upload(s->host.slots, &s->slots)) != SA_OK ||
-      (st = upload(s->host.band, &s->band)) != SA_OK ||
-      (st = upload(s->host.global, &s->global)) != SA_OK ||
-      (st = upload(p.globals, &s->globals)) != SA_OK) {
-    free_schedule(*s);
+  if ((st = upload(s->host.slots, &s->slots, ds.pool, stream)) != SA_OK ||
+      (st = upload(s->host.band, &s->band, ds.pool, stream)) != SA_OK ||
+      (st = upload(s->host.global, &s->global, ds.pool, stream)) != SA_OK ||
+      (st = upload(s->host.globals_sorted, &s->globals, ds.pool, stream)) != SA_OK) {
+    free_schedule(*s, stream);
     return st;
   }
+  // later calls may come on other streams: the upload has to be complete
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    free_schedule(*s, stream);
+    return cuda_fail(e, "upload of the schedule");
+  }
+  s->active = 1;
   *out = s.get();
   ds.schedules[key] = std::move(s);
   return SA_OK;
 }
 
+// Hands a schedule back after the call's work on `stream` is enqueued: an event
+// recorded there marks when the device is done reading it.  Takes g_mutex.
+void release_schedule(DeviceState &ds, DeviceSchedule &s, cudaStream_t stream, bool capturing) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  s.active -= 1;
+  if (capturing) {
+    s.captured = true;
+    return;
+  }
+  prune_events(ds, s);
+  cudaEvent_t ev = nullptr;
+  if (!ds.spare_events.empty()) {
+    ev = ds.spare_events.back();
+    ds.spare_events.pop_back();
+  } else if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+    s.captured = true;  // cannot track its last use: keep it
+    return;
+  }
+  if (cudaEventRecord(ev, stream) != cudaSuccess) {
+    ds.spare_events.push_back(ev);
+    s.captured = true;
+    return;
+  }
+  s.inflight.push_back(ev);
+}
+
 // ---------------------------------------------------------------------------
-// profiling events
+// profiling events (a lock of their own: launches happen outside g_mutex)
 
 struct ProfileRecord {
   int stage;
+  int launches;  // kernel launches between the two events
   cudaEvent_t start, stop;
 };
 struct Profiler {
+  std::mutex mutex;
   bool on = false;
   std::vector<ProfileRecord> records;
   std::vector<cudaEvent_t> spare;
@@ -174,20 +281,56 @@ struct StageTimer {
   cudaStream_t stream;
   cudaEvent_t start = nullptr;
   StageTimer(int s, cudaStream_t st) : stage(s), stream(st) {
+    std::lock_guard<std::mutex> lock(g_prof.mutex);
     if (g_prof.on) {
       start = g_prof.get();
       cudaEventRecord(start, stream);
     }
   }
-  void done() {
+  void done(int launches = 1) {
     if (start) {
+      std::lock_guard<std::mutex> lock(g_prof.mutex);
       cudaEvent_t stop = g_prof.get();
       cudaEventRecord(stop, stream);
-      g_prof.records.push_back({stage, start, stop});
+      g_prof.records.push_back({stage, launches, start, stop});
       start = nullptr;
     }
   }
 };
+
+// ---------------------------------------------------------------------------
+// precision of the P V product on the bf16 tensor-core path
+
+std::atomic<int> g_pv_mode{SA_PV_AUTO};
+
+// Automatic choice: split P into two bf16 parts when the softmax of some row
+// can concentrate on a few keys, where the rounding of single bf16 weights no
+// longer averages out -- rows with fewer than kSplitMinKeys keys, or a score
+// scale |scale| sqrt(D) above kSplitMaxScale (unit-variance q and k give
+// scores of standard deviation |scale| sqrt(D)).
+constexpr int kSplitMinKeys = 128;
+constexpr float kSplitMaxScale = 1.25f;
+
+bool split_p(const Problem &p) {
+  const int mode = g_pv_mode.load(std::memory_order_relaxed);
+  if (mode == SA_PV_SINGLE) return false;
+  if (mode == SA_PV_SPLIT) return true;
+  if (std::fabs(p.scale) * std::sqrt((float)p.D) > kSplitMaxScale) return true;
+  // fewest keys of a non-global row: a band row at the sequence edge sees
+  // half + 1 keys (of its residue class); a chunk row its chunk (the last
+  // chunk may be short) plus the memory
+  int64_t min_keys;
+  if (p.chunk > 0) {
+    const int64_t main = (int64_t)p.N - p.memory;
+    const int64_t last = main > 0 ? (main % p.chunk == 0 ? p.chunk : main % p.chunk) : p.chunk;
+    min_keys = std::min<int64_t>(p.chunk, last) + p.memory;
+  } else {
+    int64_t shortest = p.N;
+    for (int d : p.dilation) shortest = std::min<int64_t>(shortest, ((int64_t)p.N + d - 1) / d);
+    min_keys = std::min<int64_t>((int64_t)p.half + 1, shortest) + (int64_t)p.globals.size();
+  }
+  return min_keys < kSplitMinKeys;
+}
 
 // ---------------------------------------------------------------------------
 
@@ -242,21 +385,36 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-
-  std::lock_guard<std::mutex> lock(g_mutex);
-  DeviceState *ds = nullptr;
-  sa_status st = device_state(dev, &ds);
-  if (st != SA_OK) return st;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  const bool capturing = cs != cudaStreamCaptureStatusNone;
 
   // bf16 -> tensor cores (kind::f16); tf32 (fp32 in memory, D = 64) -> tensor
   // cores (kind::tf32, no cast of the inputs); fp32 -> CUDA cores, fp32 throughout
   if (dtype == SA_TF32 && !tc_supports(dtype, D))
     return fail(SA_ERR_UNSUPPORTED, "SA_TF32 supports D = 64 (got %d)", D);
   const bool tc = tc_supports(dtype, D);
-  const Tiling tiling = tc ? tc_tiling(D) : kSimtTiling;
-  const DeviceSchedule *sched = nullptr;
-  st = get_schedule(*ds, p, tc ? 1 : 0, tiling, &sched);
-  if (st != SA_OK) return st;
+  const bool precise = tc && dtype == SA_BF16 && split_p(p);
+
+  DeviceState *ds = nullptr;
+  DeviceSchedule *sched = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    sa_status st = device_state(dev, &ds);
+    if (st != SA_OK) return st;
+    const Tiling tiling = tc ? tc_tiling(D, ds->sms) : kSimtTiling;
+    st = acquire_schedule(*ds, p, tc ? 1 : 0, tiling, stream, capturing, &sched);
+    if (st != SA_OK) return st;
+  }
+  // the schedule is handed back once everything is enqueued, on every path
+  struct Release {
+    DeviceState *ds;
+    DeviceSchedule *s;
+    cudaStream_t stream;
+    bool capturing;
+    ~Release() { release_schedule(*ds, *s, stream, capturing); }
+  } release{ds, sched, stream, capturing};
   const Schedule &hs = sched->host;
 
   DevProblem dp{};
@@ -291,12 +449,16 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   dp.n_gitems = (int)hs.global.size();
   dp.n_chunks = hs.n_chunks;
   dp.chunk_len = hs.chunk_len;
+  dp.part_sets = hs.part_sets;
+  dp.part_sub = hs.part_sub;
+  dp.g_alt = hs.g_alt ? 1 : 0;
+  dp.g_packed = hs.g_packed ? 1 : 0;
   dp.err = ds->err;
 
   const int BH = B * H;
   const size_t esize = dtype == SA_BF16 ? 2 : 4;
   const size_t g_rows = (size_t)BH * hs.g_pad * D;
-  const size_t part_rows = (size_t)BH * hs.n_chunks * hs.g_pad;
+  const size_t part_rows = (size_t)BH * hs.part_sets * hs.g_pad;
   size_t off_q = 0, off_k = 0, off_v = 0, off_po = 0, off_ml = 0, total = 0;
   auto carve = [&total](size_t bytes) {
     size_t at = total;
@@ -304,9 +466,11 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
     return at;
   };
   if (dp.n_g > 0) {
-    off_q = carve(g_rows * esize);
-    off_k = carve(g_rows * esize);
-    off_v = carve(g_rows * esize);
+    if (dp.g_first < 0) {
+      off_q = carve(g_rows * esize);
+      off_k = carve(g_rows * esize);
+      off_v = carve(g_rows * esize);
+    }
     off_po = carve(part_rows * D * sizeof(float));
     off_ml = carve(part_rows * 2 * sizeof(float));
   }
@@ -328,9 +492,11 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
     e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&scratch), total, ds->pool, stream);
     if (e != cudaSuccess)
       return fail(SA_ERR_NO_MEMORY, "scratch of %zu bytes: %s", total, cudaGetErrorString(e));
-    dp.qg = scratch + off_q;
-    dp.kg = scratch + off_k;
-    dp.vg = scratch + off_v;
+    if (dp.g_first < 0) {
+      dp.qg = scratch + off_q;
+      dp.kg = scratch + off_k;
+      dp.vg = scratch + off_v;
+    }
     dp.part_o = reinterpret_cast<float *>(scratch + off_po);
     dp.part_ml = reinterpret_cast<float *>(scratch + off_ml);
     if (tf32) {
@@ -343,17 +509,20 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   }
 
   sa_status result = SA_OK;
-  auto step = [&](int stage, auto &&launch, const char *what) {
+  auto step = [&](int stage, const char *range, auto &&launch, const char *what,
+                  int launches = 1) {
     if (result != SA_OK) return;
+    nvtxRangePushA(range);
     StageTimer timer(stage, stream);
     cudaError_t le = launch();
-    timer.done();
+    timer.done(launches);
+    nvtxRangePop();
     if (le != cudaSuccess) result = cuda_fail(le, what);
   };
   if (dp.n_g > 0 && dp.g_first < 0)
-    step(0, [&] { return launch_gather(dp, BH, dtype, stream); }, "gather launch");
+    step(0, "sa.gather", [&] { return launch_gather(dp, BH, dtype, stream); }, "gather launch");
   if (tf32) {
-    step(0, [&] {
+    step(0, "sa.transpose_values", [&] {
       size_t off = 0;
       for (const Slot &sl : hs.slots) {
         const int lp = values_len_pad(sl.len);
@@ -371,19 +540,25 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
                                        std::min(hs.g_pad, N - dp.g_first), hs.g_pad, BH, stream);
       return launch_transpose_values(static_cast<const float *>(dp.vg), dp.vgT, hs.g_pad, D, 0, 1,
                                      hs.g_pad, hs.g_pad, BH, stream);
-    }, "value transposition launch");
+    }, "value transposition launch", (int)hs.slots.size() + (dp.n_g > 0 ? 2 : 0));
   }
+  // tensor cores: the global-row items run on CTAs of the band launch when
+  // the schedule assigns them some (hs.g_ctas), else in a launch of their own
+  const bool fused = tc && dp.n_g > 0 && hs.g_ctas > 0;
   if (tc)
-    step(1, [&] { return launch_band_tc(dp, dtype, hs.slots.data(), (int)hs.slots.size(), hs.group_begin, BH, stream); },
-         "band (tensor-core) launch");
+    step(1, fused ? "sa.band+global_rows" : "sa.band", [&] {
+      return launch_band_tc(dp, dtype, precise, hs.slots.data(), (int)hs.slots.size(), hs.group_begin,
+                            BH, ds->sms, fused ? hs.g_ctas : 0, hs.band_ctas, stream);
+    }, "band (tensor-core) launch", (int)hs.group_begin.size() - 1);
   else
-    step(1, [&] { return launch_band_simt(dp, dtype, stream); }, "band launch");
+    step(1, "sa.band", [&] { return launch_band_simt(dp, dtype, stream); }, "band launch");
   if (dp.n_g > 0) {
-    if (tc)
-      step(2, [&] { return launch_global_tc(dp, dtype, BH, stream); }, "global-row (tensor-core) launch");
-    else
-      step(2, [&] { return launch_global_simt(dp, dtype, stream); }, "global-row launch");
-    step(3, [&] { return launch_merge(dp, BH, dtype, stream); }, "merge launch");
+    if (tc && !fused)
+      step(2, "sa.global_rows", [&] { return launch_global_tc(dp, dtype, precise, BH, ds->sms, stream); },
+           "global-row (tensor-core) launch");
+    else if (!tc)
+      step(2, "sa.global_rows", [&] { return launch_global_simt(dp, dtype, stream); }, "global-row launch");
+    step(3, "sa.merge", [&] { return launch_merge(dp, BH, dtype, stream); }, "merge launch");
   }
   if (scratch) {
     e = cudaFreeAsync(scratch, stream);
@@ -582,7 +757,7 @@ extern "C" sa_status sa_sync_status(sa_stream_t stream) {
 }
 
 extern "C" sa_status sa_profile_begin(void) {
-  std::lock_guard<std::mutex> lock(g_mutex);
+  std::lock_guard<std::mutex> lock(g_prof.mutex);
   for (auto &r : g_prof.records) {
     g_prof.spare.push_back(r.start);
     g_prof.spare.push_back(r.stop);
@@ -593,7 +768,7 @@ extern "C" sa_status sa_profile_begin(void) {
 }
 
 extern "C" sa_status sa_profile_end(sa_profile *out) {
-  std::lock_guard<std::mutex> lock(g_mutex);
+  std::lock_guard<std::mutex> lock(g_prof.mutex);
   g_prof.on = false;
   sa_profile res{};
   sa_status st = SA_OK;
@@ -602,7 +777,7 @@ extern "C" sa_status sa_profile_end(sa_profile *out) {
     float ms = 0.f;
     if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
     if (e != cudaSuccess && st == SA_OK) st = cuda_fail(e, "profile event");
-    res.launches[r.stage] += 1;
+    res.launches[r.stage] += r.launches;
     res.ms[r.stage] += ms;
     g_prof.spare.push_back(r.start);
     g_prof.spare.push_back(r.stop);
@@ -612,4 +787,37 @@ extern "C" sa_status sa_profile_end(sa_profile *out) {
   return st;
 }
 
-extern "C" const char *sa_version(void) { return "sa-gb300 0.1 (sm_103a)"; }
+extern "C" sa_status sa_set_pv_mode(sa_pv_mode mode) {
+  if (mode != SA_PV_AUTO && mode != SA_PV_SINGLE && mode != SA_PV_SPLIT)
+    return fail(SA_ERR_INVALID_ARG, "unknown P V mode %d", (int)mode);
+  g_pv_mode.store((int)mode, std::memory_order_relaxed);
+  return SA_OK;
+}
+
+extern "C" sa_pv_mode sa_get_pv_mode(void) {
+  return (sa_pv_mode)g_pv_mode.load(std::memory_order_relaxed);
+}
+
+extern "C" int sa_uses_split_p(int N, int D, int window, const int32_t *dilation, int H,
+                               const int32_t *global_idx, int n_global, int chunk, int n_memory,
+                               float scale) {
+  Problem p;
+  p.B = 1;
+  p.H = H < 1 ? 1 : H;
+  p.N = N;
+  p.D = D;
+  p.window = window;
+  p.half = window / 2;
+  if (dilation && H >= 1)
+    p.dilation.assign(dilation, dilation + H);
+  else
+    p.dilation.assign(p.H, 1);
+  p.scale = scale;
+  p.dtype = SA_BF16;
+  p.chunk = chunk;
+  p.memory = n_memory;
+  if (global_idx && n_global > 0) p.globals = global_set(global_idx, n_global);
+  return split_p(p) ? 1 : 0;
+}
+
+extern "C" const char *sa_version(void) { return "sa-gb300 0.2 (sm_103a)"; }

@@ -85,8 +85,14 @@ struct Tiling {
   int key_tile;     // keys per band tile
   int g_tile;       // the gathered global rows are padded to a multiple of this
   int g_item_rows;  // global query rows per CTA of the global-row pass
-  int target_ctas;  // CTAs wanted for the global-row pass
+  int target_ctas;  // CTAs wanted for the global-row pass (separate launch)
   int max_slots;    // residue classes one launch can address (groups items)
+  // Tensor-core family: the global-row work runs on CTAs of its own inside the
+  // band launch (one CTA per SM, `sms` SMs), each query tile of such a CTA
+  // taking every other key tile of the chunk (two chains of dependent MMAs per
+  // SM); at most 64 global rows are packed two key halves to a 128-row tile.
+  int sms = 0;
+  bool fuse_global = false;
 };
 
 // Full launch schedule of one problem for one tiling.
@@ -97,7 +103,16 @@ struct Schedule {
   std::vector<int32_t> group_begin;    // band[group_begin[g] .. group_begin[g+1])
   std::vector<GlobalItem> global;
   int n_chunks = 0, chunk_len = 0, g_pad = 0;
+  // Global-row partials: sets per head (key chunks, or two per chunk when the
+  // two query tiles of a CTA take alternate key tiles), and rows per global
+  // within a set (2 when the global rows are packed: one partial per key half).
+  int part_sets = 0, part_sub = 1;
+  bool g_alt = false, g_packed = false;
+  // CTAs of the band launch that run global-row items (0: a separate launch)
+  // and the CTAs that run band items.
+  int g_ctas = 0, band_ctas = 0;
   int64_t band_tile_pairs = 0;  // executed (query tile, key tile) pairs
+  std::vector<int32_t> globals_sorted;  // the global set the schedule was built for
 };
 
 // Host scheduler (sa_schedule.cpp).

@@ -39,6 +39,14 @@ struct DevProblem {
   const GlobalItem *gitems;
   int n_gitems;
   int n_chunks, chunk_len;
+  // Partials of the global-row pass: part_sets sets per head, each g_pad rows.
+  // Global g's partials are rows g + 64 s (s < part_sub) of every set.  With
+  // g_alt the two query tiles of a CTA take alternate key tiles of chunk c and
+  // leave sets 2c and 2c + 1 (a chunk of a single key tile leaves only 2c);
+  // with g_packed the (at most 64) global rows fill a query tile twice, rows
+  // r and r + 64 taking the first and second 64 keys of each key tile.
+  int part_sets, part_sub;
+  int g_alt, g_packed;
   // scratch
   void *qg, *kg, *vg;  // [B*H][g_pad][D] gathered global rows, input dtype
   // fp32 inputs on the tensor cores (tf32): values transposed so that the P V
@@ -46,8 +54,8 @@ struct DevProblem {
   float *vT_slots;  // per residue-class slot s, back to back: [B*H][D][len_pad(s)]
   float *vT_plain;  // [B*H][D][round_up(N, 4)] of the global-row pass's values
   float *vgT;       // [B*H][D][g_pad] of the gathered global values
-  float *part_o;       // [B*H][n_chunks][g_pad][D]  unnormalised partial outputs
-  float *part_ml;      // [B*H][n_chunks][g_pad][2]  partial (max, sum), base 2
+  float *part_o;       // [B*H][part_sets][g_pad][D]  unnormalised partial outputs
+  float *part_ml;      // [B*H][part_sets][g_pad][2]  partial (max, sum), base 2
   int *err;
 };
 

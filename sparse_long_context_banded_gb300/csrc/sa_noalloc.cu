@@ -15,6 +15,8 @@
 // which compute in fp32 for either input type.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -81,7 +83,7 @@ Layout layout_of(const Problem &p, const Schedule &s) {
   L.qg = take(g_rows * es);
   L.kg = take(g_rows * es);
   L.vg = take(g_rows * es);
-  const size_t part_rows = BH * (size_t)s.n_chunks * s.g_pad;
+  const size_t part_rows = BH * (size_t)s.part_sets * s.g_pad;
   L.part_o = take(part_rows * p.D * sizeof(float));
   L.part_ml = take(part_rows * 2 * sizeof(float));
   L.total = at;
@@ -158,7 +160,8 @@ extern "C" sa_status sa_forward_noalloc(const void *q, const void *k, const void
   Layout L = layout_of(p, s);
   const int g_items = p.globals.empty() ? 1 : (int)((p.globals.size() + t.g_item_rows - 1) / t.g_item_rows);
   while (L.total > kStaticScratchBytes && s.n_chunks > 1) {
-    t.target_ctas = (s.n_chunks / 2) * B * H * g_items;
+    const int64_t want = (int64_t)(s.n_chunks / 2) * B * H * g_items;
+    t.target_ctas = (int)std::min<int64_t>(want, INT32_MAX);
     s = build_schedule(p, t);
     L = layout_of(p, s);
   }
@@ -207,6 +210,10 @@ extern "C" sa_status sa_forward_noalloc(const void *q, const void *k, const void
   dp.n_gitems = (int)s.global.size();
   dp.n_chunks = s.n_chunks;
   dp.chunk_len = s.chunk_len;
+  dp.part_sets = s.part_sets;
+  dp.part_sub = s.part_sub;
+  dp.g_alt = 0;  // the CUDA-core kernels: one partial set per chunk
+  dp.g_packed = 0;
   dp.qg = base + L.qg;
   dp.kg = base + L.kg;
   dp.vg = base + L.vg;

@@ -11,6 +11,8 @@
 #include <cmath>
 #include <cstdio>
 #include <numeric>
+#include <tuple>
+#include <utility>
 
 #include "sa_internal.h"
 
@@ -200,17 +202,99 @@ Schedule build_schedule(const Problem &p, const Tiling &t) {
   }
   s.group_begin[n_groups] = (int32_t)s.band.size();
 
-  // global-row pass: split the N keys into chunks so that enough CTAs run
+  // global-row pass: split the N keys into chunks
   if (n_g > 0) {
     s.g_pad = ((n_g + t.g_tile - 1) / t.g_tile) * t.g_tile;
     const int g_items = (n_g + t.g_item_rows - 1) / t.g_item_rows;
     const int64_t bh = (int64_t)p.B * p.H;
-    const int64_t max_chunks = (p.N + t.key_tile - 1) / t.key_tile;
-    int64_t want = (t.target_ctas + bh * g_items - 1) / (bh * g_items);
-    want = std::max<int64_t>(1, std::min(want, max_chunks));
-    const int64_t per = (p.N + want - 1) / want;
-    s.chunk_len = (int)(((per + t.key_tile - 1) / t.key_tile) * t.key_tile);
-    s.n_chunks = (int)((p.N + s.chunk_len - 1) / s.chunk_len);
+    const int64_t max_tiles = (p.N + t.key_tile - 1) / t.key_tile;
+    // tensor-core family: up to 128 global rows fill one query tile, so the
+    // CTA's two query tiles take alternate key tiles of the chunk instead
+    // (each leaves its own partial); up to 64 rows are packed twice into the
+    // tile, one copy per key half (each half leaves its own partial)
+    s.g_alt = t.q_tiles == 2 && n_g <= t.rows;
+    s.g_packed = s.g_alt && 2 * n_g <= t.rows;
+    const bool fused = t.fuse_global && t.sms > 1 && n_groups == 1;
+    auto chunk_of = [&](int64_t want, int64_t align) {
+      want = std::max<int64_t>(1, std::min(want, max_tiles));
+      const int64_t per = (p.N + want - 1) / want;
+      const int64_t len = ((per + align - 1) / align) * align;
+      return std::pair<int, int>((int)len, (int)((p.N + len - 1) / len));
+    };
+    if (!fused) {
+      int64_t want = (t.target_ctas + bh * g_items - 1) / (bh * g_items);
+      std::tie(s.chunk_len, s.n_chunks) = chunk_of(want, t.key_tile);
+    } else {
+      // Cost model in units of one key tile of both query tiles of a band CTA
+      // (the two chains interleave on the tensor core):
+      //   band item: max over its query tiles of the band tiles, plus the
+      //   global key tiles (64 keys: ~0.6 of a band tile);
+      //   global item: its key tiles, alternate tiles going to the two query
+      //   tiles (measured at D = 128: a key tile of global rows costs ~1,900
+      //   SM cycles, a band unit ~4,600).
+      // The band items are spread over S - X CTAs, the global items over X.
+      // The key chunks number X (or 2X), so that, with the items in head-major
+      // order, every global CTA takes one chunk of each head in turn and the
+      // global CTAs move through the heads together with the band CTAs (whose
+      // items are in head order too): the keys and values they read were
+      // loaded by the band tiles shortly before and come from L2.
+      const double kNarrow = 0.6, kGlobTile = 0.85, kMergePerPart = 0.15;
+      double band_total = 0.0, band_max = 0.0;
+      for (const BandItem &it : s.band) {
+        double c = 0.0;
+        for (int u = 0; u < 2; ++u)
+          if (it.k_hi[u] >= it.k_lo[u])
+            c = std::max(c, (it.k_hi[u] - it.k_lo[u] + 1) + kNarrow * ((n_g + 63) / 64));
+        band_total += c;
+        band_max = std::max(band_max, c);
+      }
+      const int S = t.sms;
+      const int64_t n_band = (int64_t)s.band.size();
+      const int64_t align = (s.g_alt ? 2 : 1) * (int64_t)t.key_tile;
+      double best = 1e300;
+      int best_x = 1, best_len = 0, best_nc = 0;
+      for (int x = 1; x < S; ++x) {
+        const int64_t bc = std::min<int64_t>(S - x, std::max<int64_t>(n_band, 1));
+        const double t_band =
+            n_band == 0 ? 0.0 : std::max(band_max, band_total / (double)bc + 0.5 * band_max);
+        for (int m = 1; m <= 2; ++m) {
+          int len, nc;
+          std::tie(len, nc) = chunk_of((int64_t)x * m, align);
+          const int64_t n_gi = bh * nc * g_items;
+          if (n_gi < x) continue;  // a global CTA without work
+          // CTA k runs items k, k + x, ...: the most key tiles any CTA runs
+          auto item_cost = [&](int c) {
+            const int64_t keys = std::min<int64_t>(p.N, (int64_t)(c + 1) * len) - (int64_t)c * len;
+            const int64_t tiles = (keys + t.key_tile - 1) / t.key_tile;
+            return kGlobTile * (double)(s.g_alt ? (tiles + 1) / 2 : tiles);
+          };
+          double t_glob = 0.0;
+          if (n_gi <= 16 * (int64_t)S) {
+            std::vector<double> per_cta(x, 0.0);
+            for (int64_t i = 0; i < n_gi; ++i) per_cta[i % x] += item_cost((int)((i / g_items) % nc));
+            t_glob = *std::max_element(per_cta.begin(), per_cta.end());
+          } else {  // many items per CTA: the average plus one item
+            double sum = 0.0;
+            for (int c = 0; c < nc; ++c) sum += item_cost(c);
+            t_glob = sum * (double)(bh * g_items) / x + item_cost(0);
+          }
+          const double tot = std::max(t_band, t_glob) +
+                             kMergePerPart * nc * (s.g_alt ? 2 : 1) * (s.g_packed ? 2 : 1);
+          if (tot < best) {
+            best = tot;
+            best_x = x;
+            best_len = len;
+            best_nc = nc;
+          }
+        }
+      }
+      s.chunk_len = best_len;
+      s.n_chunks = best_nc;
+      s.g_ctas = best_x;
+      s.band_ctas = (int)std::min<int64_t>(S - best_x, n_band);
+    }
+    s.part_sets = s.n_chunks * (s.g_alt ? 2 : 1);
+    s.part_sub = s.g_packed ? 2 : 1;
     for (int64_t x = 0; x < bh; ++x)
       for (int c = 0; c < s.n_chunks; ++c)
         for (int gt = 0; gt < g_items; ++gt)

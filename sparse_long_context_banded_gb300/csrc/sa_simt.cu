@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(NT) global_simt_kernel(DevProblem p) {
                  [&](int c) { return row_ok && t0 + c < key_hi; }, st_);
   }
   if (row_ok) {
-    const int64_t slot = ((int64_t)it.bh * p.n_chunks + it.chunk) * p.g_pad + g;
+    const int64_t slot = ((int64_t)it.bh * p.part_sets + it.chunk) * p.g_pad + g;
 #pragma unroll
     for (int j = 0; j < D / 4; ++j) p.part_o[slot * D + qd * (D / 4) + j] = st_.acc[j];
     if (qd == 0) {
@@ -268,44 +268,75 @@ constexpr int kMaxMergeChunks = 1024;
 
 template <typename T>
 __global__ void merge_kernel(DevProblem p) {
-  // One block per (global row, head).  The chunks' (max, sum) pairs are read
-  // once, in parallel, and reduced across the block; each thread then sums its
-  // output columns over the chunks with independent loads.
-  __shared__ float w_chunk[kMaxMergeChunks];
+  // One block per (global row, head), one thread per output column.  Partial x
+  // is row g + 64 (x % part_sub) of set x / part_sub.  The odd set of a chunk
+  // holding a single key tile was never written (g_alt), and a partial that
+  // saw no key has max -inf and sum 0: both get weight 0.  The partial rows'
+  // (max, sum) pairs are read once, in parallel; then every thread sums its
+  // column over the partials, eight independent loads at a time (a partial of
+  // weight 0 is loaded from a written row and discarded).
+  __shared__ float w_part[kMaxMergeChunks];
+  __shared__ int64_t row_part[kMaxMergeChunks];
   __shared__ float red[4];
-  const int g = blockIdx.x, bh = blockIdx.y, t = threadIdx.x;
-  const int64_t first = ((int64_t)bh * p.n_chunks) * p.g_pad + g;
-  const int64_t step = p.g_pad;
-  const int nc = p.n_chunks;
-  // maximum over the chunks
+  const int g = blockIdx.x, bh = blockIdx.y, t = threadIdx.x, nt = blockDim.x, nw = nt >> 5;
+  const int np = p.part_sets * p.part_sub;
+  const int64_t row0 = (int64_t)bh * p.part_sets * p.g_pad + g;  // set 0, first sub-row: written
   float m = -INFINITY;
-  for (int c = t; c < nc; c += blockDim.x) m = fmaxf(m, p.part_ml[(first + c * step) * 2]);
+  for (int x = t; x < np; x += nt) {
+    const int set = x / p.part_sub, sub = x - set * p.part_sub;
+    bool written = true;
+    if (p.g_alt && (set & 1)) {
+      const int c = set >> 1;
+      written = min(p.N, (c + 1) * p.chunk_len) - c * p.chunk_len > 128;
+    }
+    const int64_t r = row0 + (int64_t)set * p.g_pad + 64 * sub;
+    row_part[x] = written ? r : row0;
+    const float mx = written ? p.part_ml[r * 2] : -INFINITY;
+    w_part[x] = mx;
+    m = fmaxf(m, mx);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((t & 31) == 0) red[t >> 5] = m;
   __syncthreads();
-  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  m = red[0];
+  for (int i = 1; i < nw; ++i) m = fmaxf(m, red[i]);
   __syncthreads();
-  // chunk weights and the total sum
   float l = 0.f;
-  for (int c = t; c < nc; c += blockDim.x) {
-    const int64_t s = first + c * step;
-    const float wc = exp2f(p.part_ml[s * 2] - m);
-    w_chunk[c] = wc;
-    l += p.part_ml[s * 2 + 1] * wc;
+  for (int x = t; x < np; x += nt) {
+    const float mx = w_part[x];
+    const float wc = mx == -INFINITY ? 0.f : exp2f(mx - m);
+    if (wc != 0.f) l += p.part_ml[row_part[x] * 2 + 1] * wc;
+    w_part[x] = wc;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   if ((t & 31) == 0) red[t >> 5] = l;
   __syncthreads();
-  l = red[0] + red[1] + red[2] + red[3];
+  l = red[0];
+  for (int i = 1; i < nw; ++i) l += red[i];
   const float inv = 1.f / l;
   const int64_t orow = ((int64_t)bh * p.N + p.globals[g]) * p.D;
-  for (int d = t; d < p.D; d += blockDim.x) {
-    float o = 0.f;
-#pragma unroll 8
-    for (int c = 0; c < nc; ++c) o += p.part_o[(first + c * step) * p.D + d] * w_chunk[c];
-    st<T>(p.out, orow + d, o * inv);
+  // the same partials in the same order for every column and every call
+  for (int d = t; d < p.D; d += nt) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int x = 0;
+    for (; x + 8 <= np; x += 8) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = p.part_o[row_part[x + k] * p.D + d];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float wk = w_part[x + k];
+        acc[k & 3] += wk != 0.f ? v[k] * wk : 0.f;
+      }
+    }
+    for (; x < np; ++x) {
+      const float wk = w_part[x];
+      const float vk = p.part_o[row_part[x] * p.D + d];
+      acc[0] += wk != 0.f ? vk * wk : 0.f;
+    }
+    st<T>(p.out, orow + d, ((acc[0] + acc[1]) + (acc[2] + acc[3])) * inv);
   }
   if (p.lse && t == 0)
     p.lse[(int64_t)bh * p.N + p.globals[g]] = (m + log2f(l)) * 0.6931471805599453f;
@@ -384,12 +415,13 @@ cudaError_t launch_global_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s)
 }
 
 cudaError_t launch_merge(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s) {
-  if (p.n_chunks > kMaxMergeChunks) return cudaErrorInvalidValue;
+  if (p.part_sets * p.part_sub > kMaxMergeChunks) return cudaErrorInvalidValue;
   dim3 grid(p.n_g, BH);
+  const int threads = p.D;  // one thread per output column (64 or 128)
   if (dt == SA_BF16)
-    merge_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(p);
+    merge_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(p);
   else
-    merge_kernel<float><<<grid, 128, 0, s>>>(p);
+    merge_kernel<float><<<grid, threads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -74,6 +74,7 @@ struct Maps {
       o[kMaxSlotsPerLaunch];
   CUtensorMap kg, vg;  // gathered global keys / values, 64-row boxes
   CUtensorMap qg;      // gathered global queries, 128-row boxes
+  CUtensorMap qg64;    // the same, 64-row boxes (a query tile packed with two copies)
   CUtensorMap kp, vp;  // plain (undilated) keys / values, 128-row boxes
 };
 
@@ -81,8 +82,10 @@ struct Params {
   Maps maps;
   DevProblem p;
   int slot_base;    // slot index held in maps.q[0]
-  int item_offset;  // first work item of this launch
-  int n_items;      // work items of this launch (CTAs stride over them)
+  int item_offset;  // first band work item of this launch
+  int n_items;      // band work items of this launch (band CTAs stride over them)
+  int n_gctas;      // CTAs 0 .. n_gctas-1 run the global-row items instead
+  int n_gitems;     // global-row work items (those CTAs stride over them)
 };
 
 // TF: fp32 inputs on the tensor cores as tf32 (kind::tf32), else bf16 (kind::f16).
@@ -101,6 +104,11 @@ struct Cfg {
   static constexpr int kSlots = kSlots0 > 12 ? 12 : kSlots0;
   static constexpr int kSmemBytes = kQBufs * kQBytes + kSlots * kSlotBytes + kAux;
   static_assert(kSlots >= 4, "the key/value ring needs at least four slots");
+  // query buffers and ring together; a global-row CTA with one query buffer
+  // fits (kRegion - kQBytes) / kSlotBytes slots, at most kMaxSlots
+  static constexpr int kRegion = kQBufs * kQBytes + kSlots * kSlotBytes;
+  static constexpr int kMaxSlots0 = (kRegion - kQBytes) / kSlotBytes;
+  static constexpr int kMaxSlots = kMaxSlots0 > 12 ? 12 : kMaxSlots0;
 };
 
 // ---------------------------------------------------------------------------
@@ -344,6 +352,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
 }
+// Residual of a bf16 pair: (lo - bf16(lo), hi - bf16(hi)) rounded to bf16
+// pairs again, where `packed` = pack_bf16(lo, hi).  bf16(x) + residual carries
+// 16 significant bits of x.
+__device__ __forceinline__ uint32_t pack_bf16_residual(float lo, float hi, uint32_t packed) {
+  return pack_bf16(lo - __uint_as_float(packed << 16), hi - __uint_as_float(packed & 0xffff0000u));
+}
 
 // UMMA shared-memory descriptor, 128-byte swizzle (SM100 layout, version 1).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -355,6 +369,22 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 __host__ __device__ constexpr uint32_t idesc_mma(int M, int N, bool b_mn_major, bool tf32) {
   return (1u << 4) | ((tf32 ? 2u : 1u) << 7) | ((tf32 ? 2u : 1u) << 10) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Key tiles a global-row item keeps in flight to L2 ahead of its loads.
+constexpr int kGlobalAhead = 6;
+
+// L2 prefetch of the key and value tile starting at row y (128 rows).
+template <typename C>
+__device__ __forceinline__ void prefetch_kv(const CUtensorMap *mk, const CUtensorMap *mv, int y,
+                                            int bh) {
+  for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(mk, C::kHalfCols * h, y, bh);
+  if (C::kElem == 4) {
+    // transposed values (tf32): boxes of 32 keys
+    for (int c = 0; c < kKeys / 32; ++c) tma_prefetch_3d(mv, y + 32 * c, 0, bh);
+  } else {
+    for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(mv, C::kHalfCols * h, y, bh);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -415,9 +445,15 @@ __device__ __forceinline__ Work make_work(const Params &P, int item) {
     w.nb = (w.key_end - w.key0 + kKeys - 1) / kKeys;
     w.ng = 0;
     for (int u = 0; u < 2; ++u) {
-      w.active[u] = (it.g_tile * 2 + u) * kRows < p.n_g;
       w.n_lo[u] = 0;
-      w.n_cnt[u] = w.active[u] ? w.nb : 0;
+      if (p.g_alt) {
+        // one tile of global rows; query tile u takes the key tiles u, u+2, ...
+        w.active[u] = w.nb > u;
+        w.n_cnt[u] = (w.nb - u + 1) / 2;
+      } else {
+        w.active[u] = (it.g_tile * 2 + u) * kRows < p.n_g;
+        w.n_cnt[u] = w.active[u] ? w.nb : 0;
+      }
     }
   }
   return w;
@@ -426,8 +462,9 @@ __device__ __forceinline__ Work make_work(const Params &P, int item) {
 // First row of query tile u in its tensor map (class coordinate, or row of the
 // gathered global rows).
 template <bool GLOBAL>
-__device__ __forceinline__ int q_row_of(const Work &w, int u) {
-  return GLOBAL ? (w.g_tile * 2 + u) * kRows : (w.q_tile + u) * kRows;
+__device__ __forceinline__ int q_row_of(const Params &P, const Work &w, int u) {
+  if (GLOBAL) return (w.g_tile * 2 + (P.p.g_alt ? 0 : u)) * kRows;
+  return (w.q_tile + u) * kRows;
 }
 template <bool GLOBAL>
 __device__ __forceinline__ const CUtensorMap *map_q_of(const Params &P, const Work &w) {
@@ -517,7 +554,7 @@ __device__ __forceinline__ void load_scores(uint32_t t_s, bool interval, int c_l
 // on bar_half, so that the first half of P V
 // can start while the second half of P is computed; a global tile has 64 keys
 // (`narrow`) and only its first half is computed.
-template <int D, bool TF>
+template <int D, bool TF, bool PRECISE>
 __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float scale, bool interval,
                                              int c_lo, int c_hi, const int32_t *globals, int g0,
                                              int t_q, int half, bool dedup, bool narrow,
@@ -567,24 +604,46 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
     if (hh == 1 && narrow) break;
     // bf16 P: two keys per TMEM column; tf32 P (fp32 inputs): one
     constexpr int kWords = TF ? W / 2 : W / 4;
-    uint32_t pr[kWords];
+    if constexpr (PRECISE) {
+      // P = P_hi + P_lo, both bf16 (P_lo in the columns 64 on, free once S
+      // has been read): the P V product runs over both parts, so the weights
+      // it multiplies carry 16 bits, as the row sum does
+      static_assert(!TF, "split P is for bf16 inputs");
 #pragma unroll
-    for (int j = 0; j < W / 4; ++j) {
-      const int i = hh * (W / 4) + j;
-      const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
-      const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
-      sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
-      if constexpr (TF) {
-        pr[2 * j] = __float_as_uint(e.x);
-        pr[2 * j + 1] = __float_as_uint(e.y);
-      } else {
-        pr[j] = pack_bf16(e.x, e.y);
+      for (int qq = 0; qq < 2; ++qq) {
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int i = hh * (W / 4) + qq * 16 + j;
+          const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
+          const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
+          sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
+          ph[j] = pack_bf16(e.x, e.y);
+          pl[j] = pack_bf16_residual(e.x, e.y, ph[j]);
+        }
+        tmem_st16(t_s + hh * kWords + qq * 16, ph);
+        tmem_st16(t_s + 64 + hh * kWords + qq * 16, pl);
       }
+    } else {
+      uint32_t pr[kWords];
+#pragma unroll
+      for (int j = 0; j < W / 4; ++j) {
+        const int i = hh * (W / 4) + j;
+        const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
+        const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
+        sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
+        if constexpr (TF) {
+          pr[2 * j] = __float_as_uint(e.x);
+          pr[2 * j + 1] = __float_as_uint(e.y);
+        } else {
+          pr[j] = pack_bf16(e.x, e.y);
+        }
+      }
+      if constexpr (TF)
+        tmem_st64(t_s + hh * kWords, pr);
+      else
+        tmem_st32(t_s + hh * kWords, pr);
     }
-    if constexpr (TF)
-      tmem_st64(t_s + hh * kWords, pr);
-    else
-      tmem_st32(t_s + hh * kWords, pr);
     if (hh == 0) {
       tmem_wait_st();
       tc_fence_before();
@@ -598,17 +657,132 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
   m_run = m_new;
 }
 
-template <int D, bool GLOBAL, bool TF>
-__global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_constant__ Params P) {
+// Global rows packed twice into a query tile (at most 64 of them): the row
+// of this thread holds one copy of global row (row & 63) and scores only the
+// keys of its half `sub` of the key tile (S columns 64 sub .. 64 sub + 63; the
+// other copy scores the other half), keeping a running maximum and sum of its
+// own.  P of those keys goes to the half's P columns and zeros to the other
+// half's, so that the full-tile P V product adds exactly this half's keys into
+// the row's O; the two copies leave two partials of the global row.  Keys
+// past column c_hi of the half (the end of the chunk) are masked.
+template <int D, bool TF, bool PRECISE>
+__device__ __forceinline__ void softmax_packed(uint32_t t_s, uint32_t t_o, float scale, int sub,
+                                               int c_hi, float &m_run, float &l_run) {
+  constexpr int W = kKeys / 2;
+  constexpr int kWords = TF ? W : W / 2;  // P columns of one half
+  const float scl = scale;
+  float s[W];
+  {
+    uint32_t r[W];
+    tmem_ld64(t_s + sub * W, r);
+#pragma unroll
+    for (int x = 0; x < W; ++x) s[x] = __uint_as_float(r[x]);
+  }
+  {
+    // the other half's P columns (and their low parts) are zero for this row
+    uint32_t z[kWords];
+#pragma unroll
+    for (int x = 0; x < kWords; ++x) z[x] = 0u;
+    if constexpr (TF) {
+      tmem_st64(t_s + (1 - sub) * kWords, z);
+    } else {
+      tmem_st32(t_s + (1 - sub) * kWords, z);
+      if constexpr (PRECISE) tmem_st32(t_s + 64 + (1 - sub) * kWords, z);
+    }
+  }
+  if (c_hi < W - 1) {
+#pragma unroll
+    for (int x = 0; x < W; ++x) s[x] = x <= c_hi ? s[x] : -INFINITY;
+  }
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+  for (int x = 16; x < W; x += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[x + 2 * i], s[x + 2 * i + 1]);
+  const float mt =
+      max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * scl;
+  const bool need = mt > m_run + 8.f;
+  const float m_new = need ? mt : m_run;
+  const float alpha = need ? ex2(m_run - m_new) : 1.f;
+  const bool rescale = need && m_run != -INFINITY;
+  if (__any_sync(0xffffffffu, rescale)) {
+    const float a = rescale ? alpha : 1.f;
+#pragma unroll 1
+    for (int c = 0; c < D / 16; ++c) {
+      uint32_t r[16];
+      tmem_ld16(t_o + c * 16, r);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * a);
+      tmem_st16(t_o + c * 16, r);
+    }
+  }
+  const float neg = (m_new == -INFINITY) ? 0.f : -m_new;
+  const float2 scl2 = make_float2(scl, scl), neg2 = make_float2(neg, neg);
+  float2 sum2[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
+  if constexpr (PRECISE) {
+    static_assert(!TF, "split P is for bf16 inputs");
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq) {
+      uint32_t ph[16], pl[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int i = qq * 16 + j;
+        const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
+        const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
+        sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
+        ph[j] = pack_bf16(e.x, e.y);
+        pl[j] = pack_bf16_residual(e.x, e.y, ph[j]);
+      }
+      tmem_st16(t_s + sub * kWords + qq * 16, ph);
+      tmem_st16(t_s + 64 + sub * kWords + qq * 16, pl);
+    }
+  } else {
+    uint32_t pr[kWords];
+#pragma unroll
+    for (int j = 0; j < W / 2; ++j) {
+      const float2 arg = __ffma2_rn(make_float2(s[2 * j], s[2 * j + 1]), scl2, neg2);
+      const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
+      sum2[j & 3] = __fadd2_rn(sum2[j & 3], e);
+      if constexpr (TF) {
+        pr[2 * j] = __float_as_uint(e.x);
+        pr[2 * j + 1] = __float_as_uint(e.y);
+      } else {
+        pr[j] = pack_bf16(e.x, e.y);
+      }
+    }
+    if constexpr (TF)
+      tmem_st64(t_s + sub * kWords, pr);
+    else
+      tmem_st32(t_s + sub * kWords, pr);
+  }
+  const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+  const float2 s4 = __fadd2_rn(s01, s23);
+  l_run = (need ? l_run * alpha : l_run) + (s4.x + s4.y);
+  m_run = m_new;
+}
+
+template <int D, bool GLOBAL, bool TF, bool PRECISE>
+__device__ __forceinline__ void cta_body(const Params &P, const int item0, const int stride,
+                                         const int n_items) {
   using C = Cfg<D, TF>;
-  constexpr int NS = C::kSlots;
+  const DevProblem &p = P.p;
+  // Global-row CTAs whose global rows fit one query tile (g_alt) load that
+  // tile once per item for both chains, and give the space of the other query
+  // buffers to the key/value ring: their chains take alternate key tiles, so
+  // they drain the ring twice as fast as band CTAs and need it deeper.
+  const bool shared_q = GLOBAL && p.g_alt;
+  const int NQ = GLOBAL ? (shared_q ? 1 : 2) : C::kQBufs;
+  const int NS = GLOBAL ? min(C::kMaxSlots, (C::kRegion - NQ * C::kQBytes) / C::kSlotBytes) : C::kSlots;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw;
   const uint32_t s_q0 = smem_u32(smem);
-  constexpr int NQ = C::kQBufs;
   const uint32_t s_slots = s_q0 + NQ * C::kQBytes;
-  uint8_t *aux = smem + NQ * C::kQBytes + NS * C::kSlotBytes;
-  constexpr int kBars = 2 * NS + 2 * NQ + 12;
+  uint8_t *aux = smem + C::kRegion;
+  constexpr int kBars = 2 * C::kMaxSlots + 2 * C::kQBufs + 12;
   uint64_t *bar_mem = reinterpret_cast<uint64_t *>(aux);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(aux + 8 * kBars);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(aux + 8 * kBars + 4);
@@ -616,34 +790,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
   static_assert(8 * kBars + 16 <= 1024 && 1024 + 8 * SA_MAX_GLOBALS <= C::kAux, "aux layout");
   Bars B;
   B.slot_full = smem_u32(bar_mem);
-  B.slot_empty = B.slot_full + 8 * NS;
-  B.q_full = B.slot_empty + 8 * NS;  // [NQ]
-  B.q_empty = B.q_full + 8 * NQ;     // [NQ]
-  B.s_full = B.q_empty + 8 * NQ;     // [2]
+  B.slot_empty = B.slot_full + 8 * C::kMaxSlots;
+  B.q_full = B.slot_empty + 8 * C::kMaxSlots;  // [NQ]
+  B.q_empty = B.q_full + 8 * C::kQBufs;        // [NQ]
+  B.s_full = B.q_empty + 8 * C::kQBufs;        // [2]
   B.p_half = B.s_full + 16;          // [2]
   B.p_full = B.p_half + 16;          // [2]
   B.o_final = B.p_full + 16;         // [2]
   B.mma_done = B.o_final + 16;       // [2]
   B.s_issued = B.mma_done + 16;      // [2]
 
-  const DevProblem &p = P.p;
   const int tid = threadIdx.x;
   if (s_q0 & 1023u) {  // 128-byte-swizzled tiles need 1024-byte alignment
     if (tid == 0 && p.err) atomicOr(p.err, kErrBadWork);
     return;
   }
   const int warp = tid >> 5, lane = tid & 31;
-  const int n_items = P.n_items;
-  const int item0 = blockIdx.x, stride = gridDim.x;
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(B.slot_full + 8 * i, 1);
-      mbar_init(B.slot_empty + 8 * i, 2);  // one arrival per MMA issuer
+      // one arrival per MMA issuer; per reading issuer with alternating tiles
+      mbar_init(B.slot_empty + 8 * i, shared_q ? 1 : 2);
     }
     for (int b = 0; b < NQ; ++b) {
       mbar_init(B.q_full + 8 * b, 1);
-      mbar_init(B.q_empty + 8 * b, 1);
+      // a shared query tile is released by both softmax warpgroups
+      mbar_init(B.q_empty + 8 * b, shared_q ? 2 : 1);
     }
     for (int u = 0; u < 2; ++u) {
       mbar_init(B.s_full + 8 * u, 1);
@@ -678,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
       uint32_t j = 0;  // query tiles loaded so far
       bool ok = true;
       // output tile staged in each buffer: map index, first row, head
-      int out_ls[NQ], out_row[NQ], out_bh[NQ];
+      int out_ls[C::kQBufs], out_row[C::kQBufs], out_bh[C::kQBufs];
       auto store_staged = [&](uint32_t b) {
         for (int h = 0; h < C::kHalves; ++h)
           tma_store_3d(&P.maps.o[out_ls[b]], s_q0 + b * C::kQBytes + h * (kRows * 128),
@@ -693,9 +866,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           for (int u = 0; u < 2; ++u)
             if (wn.active[u])
               for (int h = 0; h < C::kHalves; ++h)
-                tma_prefetch_3d(mq, C::kHalfCols * h, q_row_of<GLOBAL>(wn, u), wn.bh);
+                tma_prefetch_3d(mq, C::kHalfCols * h, q_row_of<GLOBAL>(P, wn, u), wn.bh);
         }
         const CUtensorMap *mq = map_q_of<GLOBAL>(P, w);
+        if (shared_q) {
+          // one tile of global rows for both chains
+          const uint32_t b = j % NQ, use = j / NQ;
+          if (!wait_bar(B.q_empty + 8 * b, (use & 1u) ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(B.q_full + 8 * b, C::kQBytes);
+          if (p.g_packed) {
+            for (int h = 0; h < C::kHalves; ++h)
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d(s_q0 + b * C::kQBytes + h * (kRows * 128) + c * (kRows / 2) * 128,
+                            &P.maps.qg64, B.q_full + 8 * b, C::kHalfCols * h, 0, w.bh);
+          } else {
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_3d(s_q0 + b * C::kQBytes + h * (kRows * 128), mq, B.q_full + 8 * b,
+                          C::kHalfCols * h, q_row_of<GLOBAL>(P, w, 0), w.bh);
+          }
+          ++j;
+          continue;
+        }
         for (int u = 0; u < 2 && ok; ++u) {
           if (!w.active[u]) continue;
           const uint32_t b = j % NQ, use = j / NQ;
@@ -715,9 +909,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
             out_bh[b] = w.bh;
           }
           mbar_expect_tx(B.q_full + 8 * b, C::kQBytes);
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(s_q0 + b * C::kQBytes + h * (kRows * 128), mq, B.q_full + 8 * b, C::kHalfCols * h,
-                        q_row_of<GLOBAL>(w, u), w.bh);
+          if (GLOBAL && p.g_packed) {
+            // the (at most 64) global rows twice: rows 0-63 and 64-127 of the tile
+            for (int h = 0; h < C::kHalves; ++h)
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d(s_q0 + b * C::kQBytes + h * (kRows * 128) + c * (kRows / 2) * 128,
+                            &P.maps.qg64, B.q_full + 8 * b, C::kHalfCols * h, 0, w.bh);
+          } else {
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_3d(s_q0 + b * C::kQBytes + h * (kRows * 128), mq, B.q_full + 8 * b,
+                          C::kHalfCols * h, q_row_of<GLOBAL>(P, w, u), w.bh);
+          }
           ++j;
         }
       }
@@ -737,16 +939,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------- K/V producer
-    // (lane 0; lane 1 of this warp is the Q producer, waiting independently)
-    if (lane == 0) {
-      int n = 0;
+    // (lane 0; lane 1 of this warp is the Q producer, waiting independently).
+    // Alternating chains (global rows in one query tile) get a producer each:
+    // lane 0 loads the even key tiles (chain 0), lane 2 the odd ones (chain 1),
+    // each into its own half of the ring [c NS/2, (c+1) NS/2), so that every
+    // use of a slot belongs to the chain that waits on it (a barrier's waiter
+    // may never fall two phases behind it) and neither chain's loads queue
+    // behind the other's.
+    const bool split = GLOBAL && shared_q;
+    if (lane == 0 || (split && lane == 2)) {
+      const int chain = lane == 2 ? 1 : 0;
+      const int nsc = NS / 2;
+      int n = 0;  // loads issued by this thread
       bool ok = true;
       for (int item = item0; item < n_items && ok; item += stride) {
         const Work w = make_work<GLOBAL>(P, item);
         const CUtensorMap *map_k = GLOBAL ? &P.maps.kp : &P.maps.k[w.slot - P.slot_base];
         const CUtensorMap *map_v = GLOBAL ? &P.maps.vp : &P.maps.v[w.slot - P.slot_base];
         const int n_tiles = w.nb + w.ng;
-        for (int pos = 0; pos < n_tiles && ok; ++pos) {
+        const int first_pos = split ? chain : 0, step = split ? 2 : 1;
+        if (GLOBAL)  // the first key tiles of the item into L2 ahead of their loads
+          for (int a = first_pos; a < kGlobalAhead && a < n_tiles; a += step)
+            prefetch_kv<C>(map_k, map_v, w.key0 + a * kKeys, w.bh);
+        for (int pos = first_pos; pos < n_tiles && ok; pos += step) {
+          // global rows: each key tile serves one query tile, so tiles are
+          // consumed twice as fast as band tiles, and the ring alone cannot
+          // cover the memory latency; keep kGlobalAhead tiles on their way to L2
+          if (GLOBAL && pos + kGlobalAhead < n_tiles)
+            prefetch_kv<C>(map_k, map_v, w.key0 + (pos + kGlobalAhead) * kKeys, w.bh);
           const bool gt = is_global_pos(w, pos);
           const int bp = band_index(w, pos);
           const int rows = gt ? kGKeys : kKeys;
@@ -754,7 +974,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
           const CUtensorMap *mk = gt ? &P.maps.kg : map_k;
           const CUtensorMap *mv = gt ? &P.maps.vg : map_v;
           for (int which = 0; which < 2; ++which, ++n) {
-            const int s = n % NS, use = n / NS;
+            const int s = split ? chain * nsc + n % nsc : n % NS;
+            const int use = split ? n / nsc : n / NS;
             if (!wait_bar(B.slot_empty + 8 * s, (use & 1) ^ 1, abort_flag, p.err)) {
               ok = false;
               break;
@@ -775,8 +996,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
       }
       if (!ok) {
         // drain the loads still in flight before the CTA's memory is released
-        for (int k = max(0, n - NS); k < n; ++k)
-          wait_bar(B.slot_full + 8 * (k % NS), (k / NS) & 1, abort_flag, nullptr, false);
+        const int depth = split ? nsc : NS;
+        for (int k = max(0, n - depth); k < n; ++k) {
+          const int s = split ? chain * nsc + k % nsc : k % NS;
+          wait_bar(B.slot_full + 8 * s, (k / depth) & 1, abort_flag, nullptr, false);
+        }
       }
     }
   } else if (warp == 9 || warp == 10) {
@@ -822,14 +1046,97 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
       const uint64_t dv_glob = TF ? sw128_desc(s_slots, 16, 1024) : sw128_desc(s_slots, kGKeys * 128, 1024);
       const uint32_t d_s = tmem + u * 128, d_o = tmem + 256 + u * 128;
       const uint32_t s_full = B.s_full + 8 * u, p_full = B.p_full + 8 * u;
+      if (GLOBAL && p.g_alt) {
+        // Global rows in one query tile: chain u reads only the key tiles u,
+        // u+2, ... of each item, so this issuer visits only those -- no
+        // ping-pong hand-off, as the chains share no tile.  Chain u's loads
+        // cycle through its half of the ring (slots u NS/2 ..): the keys of
+        // its i-th tile are its load base + 2 i (values: + 1), and it alone
+        // waits on and releases those slots.
+        const int nsc = NS / 2;
+        uint32_t pv = 0, jq = 0, base = 0;
+        bool ok = true;
+        const bool one_piece = p.g_packed;  // packed rows: P arrives in one piece
+        for (int item = item0; item < n_items && ok; item += stride) {
+          const Work w = make_work<GLOBAL>(P, item);
+          const bool act = u ? w.active[1] : w.active[0];
+          const uint32_t jt = jq++;  // one shared query tile per item
+          const uint32_t qb = jt % NQ;
+          const uint64_t dq = sw128_desc(s_q0 + qb * C::kQBytes, 16, 1024);
+          const int n_u = act ? (u ? w.n_cnt[1] : w.n_cnt[0]) : 0;
+          // every item's tile is waited for, used or not: the barrier's phases
+          // are then followed one by one
+          ok = __all_sync(0xffffffffu, wait_bar(B.q_full + 8 * qb, (jt / NQ) & 1u, abort_flag, p.err));
+          if (!ok) break;
+          tc_fence_after();
+          for (int i = 0; i <= n_u && ok; ++i) {
+            if (i > 0) {
+              // P V of this chain's previous tile
+              const uint32_t nv = base + 2u * (uint32_t)(i - 1) + 1u;
+              const int v_slot = u * nsc + (int)(nv % (uint32_t)nsc);
+              const uint32_t v_par = (nv / (uint32_t)nsc) & 1u;
+              ok = __all_sync(0xffffffffu, wait_bar(one_piece ? p_full : B.p_half + 8 * u, pv & 1u, abort_flag, p.err));
+              if (ok) ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * v_slot, v_par, abort_flag, p.err));
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t off = (uint64_t)((v_slot * C::kSlotBytes) >> 4);
+              const uint32_t first = i == 1 ? 0u : 1u;
+              if (!one_piece) {
+#pragma unroll
+                for (int kk = 0; kk < kPvHalf; ++kk)
+                  mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_band + off + v_step(kk), kIdescPV,
+                                  kk > 0 ? 1u : first);
+                if constexpr (PRECISE) {
+#pragma unroll
+                  for (int kk = 0; kk < kPvHalf; ++kk)
+                    mma_ts_warp<TF>(d_o, d_s + 64 + kk * 8, dv_band + off + v_step(kk), kIdescPV, 1u);
+                }
+                ok = __all_sync(0xffffffffu, wait_bar(p_full, pv & 1u, abort_flag, p.err));
+                if (!ok) break;
+                tc_fence_after();
+              }
+#pragma unroll
+              for (int kk = one_piece ? 0 : kPvHalf; kk < 2 * kPvHalf; ++kk)
+                mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_band + off + v_step(kk), kIdescPV,
+                                kk > 0 ? 1u : first);
+              if constexpr (PRECISE) {
+#pragma unroll
+                for (int kk = one_piece ? 0 : kPvHalf; kk < 2 * kPvHalf; ++kk)
+                  mma_ts_warp<TF>(d_o, d_s + 64 + kk * 8, dv_band + off + v_step(kk), kIdescPV, 1u);
+              }
+              ++pv;
+              mma_commit_warp(B.slot_empty + 8 * v_slot);
+              if (i == n_u) mma_commit_warp(B.o_final + 8 * u);
+            }
+            if (i < n_u) {
+              // S of this chain's next tile
+              const uint32_t nk = base + 2u * (uint32_t)i;
+              const int k_slot = u * nsc + (int)(nk % (uint32_t)nsc);
+              const uint32_t k_par = (nk / (uint32_t)nsc) & 1u;
+              ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * k_slot, k_par, abort_flag, p.err));
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < D / C::kMmaK; ++kk)
+                mma_ss_warp<TF>(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                                dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
+              mma_commit_warp(s_full);
+              mma_commit_warp(B.slot_empty + 8 * k_slot);
+            }
+          }
+          base += 2u * (uint32_t)(u ? w.n_cnt[1] : w.n_cnt[0]);
+        }
+      }
       uint32_t pv = 0, jq = 0, g = 0;  // jq: query tiles of earlier items
       int k_slot = 0, k_par = 0;  // ring position and phase of the next K load
-      bool ok = true;
+      bool ok = !(GLOBAL && p.g_alt);  // (the alternating issuer above has run instead)
       for (int item = item0; item < n_items && ok; item += stride) {
         const Work w = make_work<GLOBAL>(P, item);
         const bool act = u ? w.active[1] : w.active[0];
-        const uint32_t jt = jq + ((u == 1 && w.active[0]) ? 1u : 0u);  // this tile's load index
-        jq += (uint32_t)w.active[0] + (uint32_t)w.active[1];
+        // this tile's load index (a shared tile: one load per item)
+        const uint32_t jt = shared_q ? jq : jq + ((u == 1 && w.active[0]) ? 1u : 0u);
+        jq += shared_q ? 1u : (uint32_t)w.active[0] + (uint32_t)w.active[1];
         const uint32_t qb = jt % NQ;
         const uint64_t dq = sw128_desc(s_q0 + qb * C::kQBytes, 16, 1024);
         if (act) {
@@ -874,22 +1181,39 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
               tc_fence_after();
               const uint64_t off = (uint64_t)((v_slot * C::kSlotBytes) >> 4);
               const uint32_t first = pv_item == 0 ? 0u : 1u;
+              // split P (PRECISE): the low parts sit 64 columns after the high
+              // parts and multiply the same value rows
               if (!gp) {
 #pragma unroll
                 for (int kk = 0; kk < kPvHalf; ++kk)
                   mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_band + off + v_step(kk), kIdescPV,
                                   kk > 0 ? 1u : first);
+                if constexpr (PRECISE) {
+#pragma unroll
+                  for (int kk = 0; kk < kPvHalf; ++kk)
+                    mma_ts_warp<TF>(d_o, d_s + 64 + kk * 8, dv_band + off + v_step(kk), kIdescPV, 1u);
+                }
                 ok = __all_sync(0xffffffffu, wait_bar(p_full, pv & 1u, abort_flag, p.err));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = kPvHalf; kk < 2 * kPvHalf; ++kk)
                   mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_band + off + v_step(kk), kIdescPV, 1u);
+                if constexpr (PRECISE) {
+#pragma unroll
+                  for (int kk = kPvHalf; kk < 2 * kPvHalf; ++kk)
+                    mma_ts_warp<TF>(d_o, d_s + 64 + kk * 8, dv_band + off + v_step(kk), kIdescPV, 1u);
+                }
               } else {
 #pragma unroll
                 for (int kk = 0; kk < kGKeys / C::kMmaK; ++kk)
                   mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_glob + off + v_step(kk), kIdescPV,
                                   kk > 0 ? 1u : first);
+                if constexpr (PRECISE) {
+#pragma unroll
+                  for (int kk = 0; kk < kGKeys / C::kMmaK; ++kk)
+                    mma_ts_warp<TF>(d_o, d_s + 64 + kk * 8, dv_glob + off + v_step(kk), kIdescPV, 1u);
+                }
               }
               ++pv;
               ++pv_item;
@@ -960,10 +1284,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     for (int item = item0; item < n_items && ok; item += stride) {
       const Work w = make_work<GLOBAL>(P, item);
       const bool act_u = u ? w.active[1] : w.active[0];
-      const uint32_t jt = jq + ((u == 1 && w.active[0]) ? 1u : 0u);  // this tile's load index
-      jq += (uint32_t)w.active[0] + (uint32_t)w.active[1];
-      if (!act_u) continue;
+      // this tile's load index (a shared tile: one load per item)
+      const uint32_t jt = shared_q ? jq : jq + ((u == 1 && w.active[0]) ? 1u : 0u);
+      jq += shared_q ? 1u : (uint32_t)w.active[0] + (uint32_t)w.active[1];
       const uint32_t qb = jt % NQ;  // buffer holding Q_u; the output is staged there
+      if (!act_u) {
+        // A shared tile is released by both warpgroups, working or not.  An
+        // idle warpgroup first waits for the item's tile to be loaded: it may
+        // not release a later use of the buffer before the current one has
+        // been released (the barrier would run a phase ahead of its waiter).
+        if (shared_q) {
+          ok = named_bar_and(bar_id, 128, wait_bar(B.q_full + 8 * qb, (jt / NQ) & 1u, abort_flag, p.err));
+          if (!ok) break;
+          if (row == 0) mbar_arrive(B.q_empty + 8 * qb);
+        }
+        continue;
+      }
       const int nlo_u = u ? w.n_lo[1] : w.n_lo[0];
       const int ncnt_u = u ? w.n_cnt[1] : w.n_cnt[0];
       const int n = ncnt_u + w.ng;
@@ -992,9 +1328,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
         row_keys(half, p.chunk, p.memory, w.len, q0, unused, hi_first);
         row_keys(half, p.chunk, p.memory, w.len, t_q, r_lo, r_hi);
       }
+      // packed global rows: this copy of the row scores the key half `sub`
+      const bool packed = GLOBAL && p.g_packed;
+      const int sub = row >> 6;
       float m_run = -INFINITY, l_run = 0.f;
       for (int i = 0; i < n && ok; ++i) {
-        const int pos = seq_pos_s(w, nlo_u, ncnt_u, i);
+        // global rows in one query tile: tile u takes the key tiles u, u+2, ...
+        const int pos = (GLOBAL && p.g_alt) ? 2 * i + u : seq_pos_s(w, nlo_u, ncnt_u, i);
         const bool gt = is_global_pos(w, pos);
         // the tile's masks are set up before its S is awaited
         bool interval = true;
@@ -1020,8 +1360,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
         ++scnt;
         if (!ok) break;
         tc_fence_after();
-        softmax_tile<D, TF>(t_s, t_o, sl, interval, c_lo, c_hi, g_list, g0, t_q, half,
-                        dedup, gt, B.p_half + 8 * u, lane, m_run, l_run);
+        if (packed)
+          softmax_packed<D, TF, PRECISE>(t_s, t_o, sl, sub, c_hi - sub * (kKeys / 2), m_run, l_run);
+        else
+          softmax_tile<D, TF, PRECISE>(t_s, t_o, sl, interval, c_lo, c_hi, g_list, g0, t_q, half,
+                                       dedup, gt, B.p_half + 8 * u, lane, m_run, l_run);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -1083,8 +1426,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
         named_bar_sync(bar_id, 128);
         if (row == 0) mbar_arrive(B.q_empty + 8 * qb);
       } else {
-        const int gr = q_row_of<GLOBAL>(w, u) + row;
-        const int64_t slot = ((int64_t)w.bh * p.n_chunks + w.chunk) * p.g_pad + gr;
+        // partial set of this query tile and its row there; the global row it
+        // belongs to (a packed tile holds each global row twice, rows g and
+        // g + 64, one partial per key half)
+        const int set = p.g_alt ? 2 * w.chunk + u : w.chunk;
+        const int prow = q_row_of<GLOBAL>(P, w, u) + row;
+        const int gr = packed ? (row & 63) : prow;
+        const int64_t slot = ((int64_t)w.bh * p.part_sets + set) * p.g_pad + prow;
         float4 *dst = reinterpret_cast<float4 *>(p.part_o + slot * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -1115,6 +1463,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// One launch runs both kinds of work on CTAs of their own: CTAs [0, n_gctas)
+// the global-row items (the global rows against every key, split over key
+// chunks), the others the band items.  Every CTA occupies one SM for the whole
+// launch, so the two kinds run side by side and the global rows' keys and
+// values are read while the band tiles run, not in a pass of their own.
+template <int D, bool TF, bool PRECISE>
+__global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_constant__ Params P) {
+  const int b = blockIdx.x;
+  if (b < P.n_gctas)
+    cta_body<D, true, TF, PRECISE>(P, b, P.n_gctas, P.n_gitems);
+  else
+    cta_body<D, false, TF, PRECISE>(P, b - P.n_gctas, gridDim.x - P.n_gctas, P.n_items);
 }
 
 // ---------------------------------------------------------------------------
@@ -1167,28 +1529,30 @@ cudaError_t make_map_values_t(CUtensorMap *m, const float *base, int D, uint64_t
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Persistent launch: one CTA per SM (at most one work item each), every CTA
-// striding over the launch's n_items work items.
-template <int D, bool GLOBAL, bool TF>
-cudaError_t launch(Params &P, int n_items, cudaStream_t s) {
-  if (n_items <= 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
+// Persistent launch: one CTA per SM.  The first g_ctas CTAs stride over the
+// P.n_gitems global-row items, the other band_ctas CTAs over the P.n_items band
+// items.
+template <int D, bool TF, bool PRECISE>
+cudaError_t launch(Params &P, int band_ctas, int g_ctas, cudaStream_t s) {
+  const int grid = band_ctas + g_ctas;
+  if (grid <= 0) return cudaSuccess;
   constexpr int smem = Cfg<D, TF>::kSmemBytes;
-  e = cudaFuncSetAttribute(tc_attention_kernel<D, GLOBAL, TF>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(tc_attention_kernel<D, TF, PRECISE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  P.n_items = n_items;
-  const int grid = std::min(n_items, std::max(sms, 1));
-  tc_attention_kernel<D, GLOBAL, TF><<<grid, kThreads, smem, s>>>(P);
+  P.n_gctas = g_ctas;
+  tc_attention_kernel<D, TF, PRECISE><<<grid, kThreads, smem, s>>>(P);
   return cudaGetLastError();
 }
 
 }  // namespace tc
 
-Tiling tc_tiling(int) { return Tiling{tc::kRows, 2, tc::kKeys, 128, 256, 2 * 152, tc::kMaxSlotsPerLaunch}; }
+Tiling tc_tiling(int, int sms) {
+  Tiling t{tc::kRows, 2, tc::kKeys, 128, 256, 2 * sms, tc::kMaxSlotsPerLaunch};
+  t.sms = sms;
+  t.fuse_global = true;
+  return t;
+}
 
 namespace {
 
@@ -1198,6 +1562,9 @@ cudaError_t fill_common(tc::Params &P, const DevProblem &p, int BH, bool tf) {
   std::memset(&P.maps, 0, sizeof P.maps);
   P.p = p;
   P.p.half = std::min(p.half, p.N);  // a wider window changes nothing
+  P.n_items = 0;
+  P.n_gitems = p.n_gitems;
+  P.n_gctas = 0;
   const int D = p.D;
   const uint64_t es = tf ? 4 : 2;
   const uint64_t head = (uint64_t)p.N * D * es;
@@ -1211,14 +1578,16 @@ cudaError_t fill_common(tc::Params &P, const DevProblem &p, int BH, bool tf) {
     if ((e = tc::make_map(&P.maps.kg, kv, D, rows, BH, D * es, head, tc::kGKeys, tf)) ||
         (e = tf ? tc::make_map_values_t(&P.maps.vg, p.vgT, D, p.g_pad, BH)
                 : tc::make_map(&P.maps.vg, vv, D, rows, BH, D * es, head, tc::kGKeys, tf)) ||
-        (e = tc::make_map(&P.maps.qg, qv, D, rows, BH, D * es, head, tc::kRows, tf)))
+        (e = tc::make_map(&P.maps.qg, qv, D, rows, BH, D * es, head, tc::kRows, tf)) ||
+        (e = tc::make_map(&P.maps.qg64, qv, D, rows, BH, D * es, head, tc::kRows / 2, tf)))
       return e;
   } else if (p.n_g > 0) {
     const uint64_t ghead = (uint64_t)p.g_pad * D * es;
     if ((e = tc::make_map(&P.maps.kg, p.kg, D, p.g_pad, BH, D * es, ghead, tc::kGKeys, tf)) ||
         (e = tf ? tc::make_map_values_t(&P.maps.vg, p.vgT, D, p.g_pad, BH)
                 : tc::make_map(&P.maps.vg, p.vg, D, p.g_pad, BH, D * es, ghead, tc::kGKeys, tf)) ||
-        (e = tc::make_map(&P.maps.qg, p.qg, D, p.g_pad, BH, D * es, ghead, tc::kRows, tf)))
+        (e = tc::make_map(&P.maps.qg, p.qg, D, p.g_pad, BH, D * es, ghead, tc::kRows, tf)) ||
+        (e = tc::make_map(&P.maps.qg64, p.qg, D, p.g_pad, BH, D * es, ghead, tc::kRows / 2, tf)))
       return e;
   }
   if (p.n_g > 0) {
@@ -1231,11 +1600,14 @@ cudaError_t fill_common(tc::Params &P, const DevProblem &p, int BH, bool tf) {
   return cudaSuccess;
 }
 
-template <bool GLOBAL>
-cudaError_t launch_any(tc::Params &P, int D, bool tf, int n_items, cudaStream_t s) {
-  if (tf) return tc::launch<64, GLOBAL, true>(P, n_items, s);  // fp32 inputs: D = 64 only
-  return D == 64 ? tc::launch<64, GLOBAL, false>(P, n_items, s)
-                 : tc::launch<128, GLOBAL, false>(P, n_items, s);
+cudaError_t launch_any(tc::Params &P, int D, bool tf, bool precise, int band_ctas, int g_ctas,
+                       cudaStream_t s) {
+  if (tf) return tc::launch<64, true, false>(P, band_ctas, g_ctas, s);  // fp32 inputs: D = 64 only
+  if (D == 64)
+    return precise ? tc::launch<64, false, true>(P, band_ctas, g_ctas, s)
+                   : tc::launch<64, false, false>(P, band_ctas, g_ctas, s);
+  return precise ? tc::launch<128, false, true>(P, band_ctas, g_ctas, s)
+                 : tc::launch<128, false, false>(P, band_ctas, g_ctas, s);
 }
 
 }  // namespace
@@ -1244,8 +1616,9 @@ bool tc_supports(sa_dtype dt, int D) {
   return dt == SA_BF16 ? (D == 64 || D == 128) : dt == SA_TF32 && D == 64;
 }
 
-cudaError_t launch_band_tc(const DevProblem &p, sa_dtype dt, const Slot *host_slots, int n_slots,
-                           const std::vector<int32_t> &group_begin, int BH, cudaStream_t s) {
+cudaError_t launch_band_tc(const DevProblem &p, sa_dtype dt, bool precise, const Slot *host_slots,
+                           int n_slots, const std::vector<int32_t> &group_begin, int BH, int sms,
+                           int g_ctas, int band_ctas, cudaStream_t s) {
   static thread_local tc::Params P;  // ~9 KB of tensor maps: keep it off the stack
   const bool tf = dt == SA_TF32;
   cudaError_t e = fill_common(P, p, BH, tf);
@@ -1279,8 +1652,11 @@ cudaError_t launch_band_tc(const DevProblem &p, sa_dtype dt, const Slot *host_sl
     }
     P.slot_base = first;
     P.item_offset = group_begin[g];
-    const int grid = group_begin[g + 1] - group_begin[g];
-    e = launch_any<false>(P, D, tf, grid, s);
+    P.n_items = group_begin[g + 1] - group_begin[g];
+    // the global-row CTAs run beside the first group's band CTAs
+    const int gc = g == 0 ? g_ctas : 0;
+    const int bc = gc > 0 ? std::min(band_ctas, P.n_items) : std::min(P.n_items, std::max(sms, 1));
+    e = launch_any(P, D, tf, precise, bc, gc, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -1313,14 +1689,16 @@ cudaError_t launch_stalled_wait_check(int *err, uint32_t limit_us, cudaStream_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, int BH, cudaStream_t s) {
+cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, bool precise, int BH, int sms,
+                             cudaStream_t s) {
   static thread_local tc::Params P;
   const bool tf = dt == SA_TF32;
   cudaError_t e = fill_common(P, p, BH, tf);
   if (e != cudaSuccess) return e;
   P.slot_base = 0;
   P.item_offset = 0;
-  return launch_any<true>(P, p.D, tf, p.n_gitems, s);
+  P.n_items = 0;
+  return launch_any(P, p.D, tf, precise, 0, std::min(p.n_gitems, std::max(sms, 1)), s);
 }
 
 }  // namespace sa

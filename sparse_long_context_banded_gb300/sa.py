@@ -18,6 +18,7 @@ from . import build as _build
 
 SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_TIMEOUT, SA_ERR_NO_MEMORY = range(6)
 SA_BF16, SA_FP32, SA_TF32 = 0, 1, 2
+SA_PV_AUTO, SA_PV_SINGLE, SA_PV_SPLIT = 0, 1, 2
 SA_MAX_GLOBALS = 256
 STAGES = ("gather", "band", "global_rows", "merge")
 
@@ -51,6 +52,9 @@ SIGNATURES = {
                                _VP]),
     "sa_forward_global_proj": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                     _I32P, _I32P, _I, _F, _I, _VP]),
+    "sa_set_pv_mode": (_I, [_I]),
+    "sa_get_pv_mode": (_I, []),
+    "sa_uses_split_p": (_I, [_I, _I, _I, _I32P, _I, _I32P, _I, _I, _I, _F]),
 }
 SA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -318,6 +322,27 @@ def profile_end() -> dict:
     _check(load().sa_profile_end(ctypes.byref(prof)))
     return {name: {"launches": int(prof.launches[i]), "ms": float(prof.ms[i])}
             for i, name in enumerate(STAGES)}
+
+
+def set_pv_mode(mode: int):
+    """Precision of the P V product on the bf16 tensor-core path
+    (sa_set_pv_mode): SA_PV_AUTO, SA_PV_SINGLE or SA_PV_SPLIT."""
+    _check(load().sa_set_pv_mode(int(mode)))
+
+
+def get_pv_mode() -> int:
+    return int(load().sa_get_pv_mode())
+
+
+def uses_split_p(N: int, D: int, window: int, dilation: Sequence[int] | None, H: int,
+                 globals_: Sequence[int] = (), chunk: int = 0, n_memory: int = 0,
+                 scale: Optional[float] = None) -> bool:
+    """Whether a bf16 call of this shape and scale splits P (sa_uses_split_p)."""
+    dil = None if dilation is None else _i32(dilation)
+    g = _i32(globals_)
+    sc = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    return bool(load().sa_uses_split_p(int(N), int(D), int(window), _ptr(dil), int(H), _ptr(g),
+                                       int(g.size), int(chunk), int(n_memory), sc))
 
 
 def version() -> str:

@@ -155,3 +155,29 @@ def test_last_error_is_thread_local(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         sa.load(str(tmp_path / "nope.so"))
+
+
+def test_split_p_choice(lib):
+    """Automatic precision of the P V product: the five workloads keep single
+    bf16 P; narrow windows and sharp scales split it; the setting overrides."""
+    from sparse_long_context_banded_gb300 import inputs
+    for number in (1, 2, 3, 4, 5):
+        w = inputs.workload(number)
+        assert not sa.uses_split_p(w.N, w.D, w.window, w.dilation, w.H, w.globals_,
+                                   scale=w.scale), w.describe()
+    assert sa.uses_split_p(4096, 64, 100, None, 1, [0])          # 51 keys at the edge
+    assert not sa.uses_split_p(4096, 64, 254, None, 1, [0])      # 128 keys + 1 global
+    assert sa.uses_split_p(640, 64, 128, None, 1, [5], scale=0.6)
+    assert sa.uses_split_p(640, 64, 128, None, 1, [5], scale=-0.6)
+    assert not sa.uses_split_p(640, 64, 512, None, 1, [5], scale=0.15)
+    # dilation: a residue class shorter than the window limits the keys
+    assert sa.uses_split_p(300, 64, 512, [8], 1, [])
+    try:
+        sa.set_pv_mode(sa.SA_PV_SINGLE)
+        assert sa.get_pv_mode() == sa.SA_PV_SINGLE
+        assert not sa.uses_split_p(640, 64, 128, None, 1, [5], scale=0.6)
+        sa.set_pv_mode(sa.SA_PV_SPLIT)
+        assert sa.uses_split_p(4096, 64, 1024, None, 1, [0])
+    finally:
+        sa.set_pv_mode(sa.SA_PV_AUTO)
+    assert lib.sa_set_pv_mode(7) == sa.SA_ERR_INVALID_ARG

@@ -48,16 +48,18 @@ def test_count_pairs_chunked_rejects_bad_arguments(args):
     assert e.value.status == sa.SA_ERR_INVALID_ARG
 
 
-# (*) Rows with only a handful of keys: the bf16 path rounds P to bf16 for the
-# P V product, and with so few terms that rounding no longer averages out --
-# one-token chunks with 5 memory tokens (6 keys per row) exceed the absolute
-# tolerance on ~0.03% of elements in bf16 -- so that case runs in fp32.
+# (*) Rows with only a handful of keys: single bf16 weights in the P V product
+# would not average out over so few terms (one-token chunks with 5 memory
+# tokens give 6 keys per row), so the automatic choice splits P into two bf16
+# parts there; the case runs in bf16 and in fp32.
 GPU_CASES = [
     # B, H, N, D, memory, chunk, dtype
     (1, 2, 1000, 128, 16, 200, "bf16"),
     (1, 2, 777, 64, 0, 128, "bf16"),
     (1, 1, 1000, 64, 37, 100, "bf16"),      # memory and chunk not tile multiples
-    (2, 1, 600, 128, 5, 1, "fp32"),         # one-token chunks: self plus memory (*)
+    (2, 1, 600, 128, 5, 1, "bf16"),         # one-token chunks: self plus memory (*)
+    (2, 1, 600, 128, 5, 1, "fp32"),
+    (2, 1, 600, 64, 5, 1, "bf16"),
     (2, 1, 600, 128, 5, 16, "bf16"),
     (1, 2, 300, 64, 0, 1000, "bf16"),       # one chunk: plain attention
     (1, 1, 200, 64, 200, 64, "bf16"),       # all memory: dense
@@ -85,3 +87,14 @@ def test_chunked_matches_oracle(oracle, case):
     got = out.float().cpu().numpy().astype(np.float64)
     assert_close(got, ref, f"chunked {case}")
     assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, f"chunked {case}")
+
+
+def test_split_choice_for_short_chunks():
+    """Chunks shorter than 128 keys (with the memory) split P automatically."""
+    sa.load()
+    assert sa.uses_split_p(600, 128, 0, None, 1, list(range(5)), chunk=1, n_memory=5)
+    assert sa.uses_split_p(600, 128, 0, None, 1, list(range(5)), chunk=16, n_memory=5)
+    # 984 main positions = 4 * 200 + 184: the shortest chunk row sees 184 + 16 keys
+    assert not sa.uses_split_p(1000, 128, 0, None, 1, list(range(16)), chunk=200, n_memory=16)
+    # 1001 main positions = 5 * 200 + 1: the last chunk row sees 1 + 16 keys
+    assert sa.uses_split_p(1017, 64, 0, None, 1, list(range(16)), chunk=200, n_memory=16)

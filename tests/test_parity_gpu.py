@@ -90,9 +90,14 @@ def test_small_full(case, oracle):
 
 
 # A scale several times 1/sqrt(D) makes each row's softmax peak on a few keys,
-# where the bf16 rounding of P no longer averages out (as for rows with few
-# keys); such scales run through the fp32 path.
+# where single bf16 weights in the P V product no longer average out (as for
+# rows with few keys): the automatic choice splits P into two bf16 parts for
+# |scale| sqrt(D) > 1.25, and the bf16 path meets the tolerance there too.
 SCALE_CASES = [
+    (1, 1, 640, 64, 128, [1], [5], "bf16", 0.6),                 # large positive scale
+    (1, 2, 1000, 128, 256, [1, 2], [0, 999], "bf16", 0.5),
+    (1, 1, 700, 64, 300, [1], [3], "bf16", -1.0),
+    (1, 1, 2000, 128, 1024, [1], list(range(64)), "bf16", 0.3),
     # B, H, N, D, window, dilation, globals, dtype, scale
     (1, 2, 1000, 128, 256, [1, 2], [0, 999], "bf16", -0.0883),   # negative scale
     (1, 1, 700, 64, 300, [1], [3], "bf16", -0.125),
@@ -139,6 +144,59 @@ def test_tf32_full(case, oracle):
     ref, ref_lse = oracle.forward_longformer(q, k, v, window, dil, G)
     assert_close(got, ref, "tf32 " + str(case))
     assert_lse_close(got_lse, ref_lse, "tf32 " + str(case))
+
+
+# Both precisions of the P V product on the bf16 tensor-core path, whatever
+# the automatic choice would be: single bf16 P (the workloads' setting) and P
+# split into two bf16 parts.  The global sets cover every layout of the
+# global-row work: none; up to 64 rows (packed twice into a query tile, one
+# copy per key half); 65-128 rows (one query tile, the CTA's two tiles taking
+# alternate key tiles); more than 128 (two query tiles over the same keys).
+PV_CASES = [
+    # B, H, N, D, window, dilation, globals (a count: scattered; a list), dtype
+    (1, 2, 900, 64, 128, [1, 3], [], "bf16"),
+    (1, 2, 2000, 128, 512, [1, 1], list(range(64)), "bf16"),
+    (1, 1, 4096, 128, 1024, [1], [0], "bf16"),
+    (1, 2, 1500, 64, 256, [1, 2], list(range(100)), "bf16"),
+    (1, 1, 1300, 128, 300, [1], 90, "bf16"),
+    (1, 1, 3000, 64, 200, [2], 150, "bf16"),
+    (2, 1, 333, 128, 64, [1], 7, "bf16"),
+]
+
+
+@pytest.mark.parametrize("mode", ["single", "split"])
+@pytest.mark.parametrize("case", PV_CASES, ids=lambda c: "B{}H{}N{}D{}w{}d{}g{}".format(
+    c[0], c[1], c[2], c[3], c[4], max(c[5]), c[6] if isinstance(c[6], int) else len(c[6])))
+def test_pv_modes(case, mode, oracle):
+    B, H, N, D, window, dil, G, dtype = case
+    if isinstance(G, int):
+        G = sorted(np.random.default_rng(N + G).choice(N, G, replace=False).tolist())
+    q, k, v = make(B, H, N, D, dtype, seed=zlib.crc32(repr(case).encode()))
+    sa.set_pv_mode(sa.SA_PV_SINGLE if mode == "single" else sa.SA_PV_SPLIT)
+    try:
+        got, got_lse = run_gpu(q, k, v, window, dil, G)
+    finally:
+        sa.set_pv_mode(sa.SA_PV_AUTO)
+    ref, ref_lse = oracle.forward_longformer(q, k, v, window, dil, G)
+    assert_close(got, ref, f"{mode} {case}")
+    assert_lse_close(got_lse, ref_lse, f"{mode} {case}")
+
+
+def test_split_p_error_smaller_on_sharp_rows(oracle):
+    """On a sharp softmax, splitting P brings the bf16 output error down to the
+    bf16 rounding of the output itself."""
+    q, k, v = make(1, 1, 640, 64, "bf16", seed=77)
+    errs = {}
+    for mode in (sa.SA_PV_SINGLE, sa.SA_PV_SPLIT):
+        sa.set_pv_mode(mode)
+        try:
+            got, _ = run_gpu(q, k, v, 128, [1], [5], 0.6)
+        finally:
+            sa.set_pv_mode(sa.SA_PV_AUTO)
+        ref, _ = oracle.forward_longformer(q, k, v, 128, [1], [5], scale=0.6, want_lse=False)
+        errs[mode] = np.abs(got - ref) / (1e-3 + np.abs(ref))
+    assert errs[sa.SA_PV_SPLIT].max() < errs[sa.SA_PV_SINGLE].max()
+    assert errs[sa.SA_PV_SPLIT].max() < 1.0 / 128  # within an output rounding (2^-8) and a bit
 
 
 def test_tf32_rejects_d128():
@@ -262,20 +320,33 @@ def test_profile_counts_launches():
     import torch
     q, k, v = make(1, 1, 512, 64, "bf16", seed=6)
     tq, tk, tv = (to_device(a, torch) for a in (q, k, v))
-    # scattered globals: gather, band, global rows, merge
+    # scattered globals: gather, then band tiles and global rows in one
+    # tensor-core launch, then the merge
     sa.profile_begin()
     for _ in range(3):
         sa.forward(tq, tk, tv, 64, None, [3, 100])
     prof = sa.profile_end()
-    assert [prof[s]["launches"] for s in sa.STAGES] == [3, 3, 3, 3]
-    assert all(prof[s]["ms"] > 0 for s in sa.STAGES)
+    assert [prof[s]["launches"] for s in sa.STAGES] == [3, 3, 0, 3]
+    assert all(prof[s]["ms"] > 0 for s in ("gather", "band", "merge"))
     # contiguous globals: read in place, nothing gathered
     sa.profile_begin()
     for _ in range(3):
         sa.forward(tq, tk, tv, 64, None, [3, 4, 5])
     prof = sa.profile_end()
-    assert [prof[s]["launches"] for s in sa.STAGES] == [0, 3, 3, 3]
+    assert [prof[s]["launches"] for s in sa.STAGES] == [0, 3, 0, 3]
     sa.profile_begin()
     sa.forward(tq, tk, tv, 64, None, [])
     prof = sa.profile_end()
     assert [prof[s]["launches"] for s in sa.STAGES] == [0, 1, 0, 0]
+    # more residue classes than one launch addresses (dilation 17: 17 classes):
+    # two band launches and the global rows in a launch of their own
+    sa.profile_begin()
+    sa.forward(tq, tk, tv, 64, [17], [3, 4, 5])
+    prof = sa.profile_end()
+    assert [prof[s]["launches"] for s in sa.STAGES] == [0, 2, 1, 1]
+    # fp32 on the CUDA cores: four kernels
+    q32 = tq.float()
+    sa.profile_begin()
+    sa.forward(q32, q32, q32, 64, None, [3, 100])
+    prof = sa.profile_end()
+    assert [prof[s]["launches"] for s in sa.STAGES] == [1, 1, 1, 1]
