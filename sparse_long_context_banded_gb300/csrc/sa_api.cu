@@ -509,8 +509,7 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   }
 
   sa_status result = SA_OK;
-  auto step = [&](int stage, const char *range, auto &&launch, const char *what,
-                  int launches = 1) {
+  auto step = [&](int stage, const char *range, auto &&launch, const char *what, int launches = 1) {
     if (result != SA_OK) return;
     nvtxRangePushA(range);
     StageTimer timer(stage, stream);

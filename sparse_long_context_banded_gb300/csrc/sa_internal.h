@@ -24,7 +24,9 @@ struct Slot {
 // coordinates, `rows` rows each) of head bh in residue class `slot`.  For query
 // tile u the key tiles k_lo[u]..k_hi[u] (inclusive, `key_tile` keys each)
 // intersect the band; flags bit u says whether any global key falls inside
-// that query tile's band reach (so the global tile must drop duplicates).
+// that query tile's band reach (so the global tile must drop duplicates), and
+// bit 2 + u whether any of the tile's rows is a global row (whose output the
+// global-row pass writes: the band kernel leaves those rows alone).
 struct BandItem {
   int32_t bh;
   int32_t slot;

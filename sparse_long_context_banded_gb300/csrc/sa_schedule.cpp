@@ -168,13 +168,12 @@ Schedule build_schedule(const Problem &p, const Tiling &t) {
             work += it.k_hi[u] - it.k_lo[u] + 1;
             s.band_tile_pairs += it.k_hi[u] - it.k_lo[u] + 1;
             // does a global key of this class fall inside the band reach?
+            // does a global row fall inside the tile?
             for (int32_t g : p.globals) {
               if ((g - r) % d != 0) continue;
               const int64_t tg = (g - r) / d;
-              if (tg >= reach_lo && tg <= reach_hi) {
-                it.flags |= 1 << u;
-                break;
-              }
+              if (tg >= reach_lo && tg <= reach_hi) it.flags |= 1 << u;
+              if (tg >= row_lo && tg <= row_hi) it.flags |= 4 << u;
             }
           }
           if (it.k_hi[0] >= it.k_lo[0] || it.k_hi[1] >= it.k_lo[1])  // not all memory rows

@@ -264,36 +264,44 @@ __global__ void __launch_bounds__(NT) global_simt_kernel(DevProblem p) {
 // One block per (global row, head); writes that global row of `out` (and lse).
 // Upper bound of the key chunks of the global-row pass (the schedule asks for
 // at most a few hundred CTAs).
-constexpr int kMaxMergeChunks = 1024;
+constexpr int kMaxMergeChunks = 1024;  // a multiple of 64 (the smallest block)
 
 template <typename T>
 __global__ void merge_kernel(DevProblem p) {
   // One block per (global row, head), one thread per output column.  Partial x
   // is row g + 64 (x % part_sub) of set x / part_sub.  The odd set of a chunk
   // holding a single key tile was never written (g_alt), and a partial that
-  // saw no key has max -inf and sum 0: both get weight 0.  The partial rows'
-  // (max, sum) pairs are read once, in parallel; then every thread sums its
-  // column over the partials, eight independent loads at a time (a partial of
-  // weight 0 is loaded from a written row and discarded).
+  // saw no key has max -inf and sum 0: both get weight 0.  Each partial's
+  // (max, sum) pair is read once, as one 8-byte load; then every thread sums
+  // its column over the partials, sixteen independent loads at a time (a
+  // partial of weight 0 is loaded from a written row and discarded).  The
+  // partials are read in full only after the kernels that write them are done
+  // (launched as a programmatic dependent: the launch itself overlaps them).
   __shared__ float w_part[kMaxMergeChunks];
   __shared__ int64_t row_part[kMaxMergeChunks];
-  __shared__ float red[4];
+  __shared__ float red[8];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int g = blockIdx.x, bh = blockIdx.y, t = threadIdx.x, nt = blockDim.x, nw = nt >> 5;
   const int np = p.part_sets * p.part_sub;
   const int64_t row0 = (int64_t)bh * p.part_sets * p.g_pad + g;  // set 0, first sub-row: written
   float m = -INFINITY;
-  for (int x = t; x < np; x += nt) {
-    const int set = x / p.part_sub, sub = x - set * p.part_sub;
-    bool written = true;
-    if (p.g_alt && (set & 1)) {
-      const int c = set >> 1;
-      written = min(p.N, (c + 1) * p.chunk_len) - c * p.chunk_len > 128;
+  float2 ml[kMaxMergeChunks / 64];  // this thread's partials x = t, t + nt, ...
+#pragma unroll
+  for (int k = 0; k < kMaxMergeChunks / 64; ++k) {
+    const int x = t + k * nt;
+    ml[k] = make_float2(-INFINITY, 0.f);
+    if (x < np) {
+      const int set = x / p.part_sub, sub = x - set * p.part_sub;
+      bool written = true;
+      if (p.g_alt && (set & 1)) {
+        const int c = set >> 1;
+        written = min(p.N, (c + 1) * p.chunk_len) - c * p.chunk_len > 128;
+      }
+      const int64_t r = row0 + (int64_t)set * p.g_pad + 64 * sub;
+      row_part[x] = written ? r : row0;
+      if (written) ml[k] = reinterpret_cast<const float2 *>(p.part_ml)[r];
+      m = fmaxf(m, ml[k].x);
     }
-    const int64_t r = row0 + (int64_t)set * p.g_pad + 64 * sub;
-    row_part[x] = written ? r : row0;
-    const float mx = written ? p.part_ml[r * 2] : -INFINITY;
-    w_part[x] = mx;
-    m = fmaxf(m, mx);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -303,11 +311,14 @@ __global__ void merge_kernel(DevProblem p) {
   for (int i = 1; i < nw; ++i) m = fmaxf(m, red[i]);
   __syncthreads();
   float l = 0.f;
-  for (int x = t; x < np; x += nt) {
-    const float mx = w_part[x];
-    const float wc = mx == -INFINITY ? 0.f : exp2f(mx - m);
-    if (wc != 0.f) l += p.part_ml[row_part[x] * 2 + 1] * wc;
-    w_part[x] = wc;
+#pragma unroll
+  for (int k = 0; k < kMaxMergeChunks / 64; ++k) {
+    const int x = t + k * nt;
+    if (x < np) {
+      const float wc = ml[k].x == -INFINITY ? 0.f : exp2f(ml[k].x - m);
+      l += wc != 0.f ? ml[k].y * wc : 0.f;
+      w_part[x] = wc;
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
@@ -321,12 +332,12 @@ __global__ void merge_kernel(DevProblem p) {
   for (int d = t; d < p.D; d += nt) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int x = 0;
-    for (; x + 8 <= np; x += 8) {
-      float v[8];
+    for (; x + 16 <= np; x += 16) {
+      float v[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = p.part_o[row_part[x + k] * p.D + d];
+      for (int k = 0; k < 16; ++k) v[k] = p.part_o[row_part[x + k] * p.D + d];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 16; ++k) {
         const float wk = w_part[x + k];
         acc[k & 3] += wk != 0.f ? v[k] * wk : 0.f;
       }
@@ -416,13 +427,20 @@ cudaError_t launch_global_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s)
 
 cudaError_t launch_merge(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s) {
   if (p.part_sets * p.part_sub > kMaxMergeChunks) return cudaErrorInvalidValue;
-  dim3 grid(p.n_g, BH);
-  const int threads = p.D;  // one thread per output column (64 or 128)
-  if (dt == SA_BF16)
-    merge_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(p);
-  else
-    merge_kernel<float><<<grid, threads, 0, s>>>(p);
-  return cudaGetLastError();
+  // one thread per output column (64 or 128); a programmatic dependent launch,
+  // so that the launch overlaps the kernels before it (the kernel waits for
+  // them with griddepcontrol.wait before it reads anything)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.n_g, BH);
+  cfg.blockDim = dim3(p.D);
+  cfg.stream = s;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (dt == SA_BF16) return cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16>, p);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<float>, p);
 }
 
 }  // namespace sa
