@@ -320,8 +320,15 @@ sa_status sa_profile_end(sa_profile *out);
  *  globals fits.)
  *
  *  Set-up: the first call on each device looks up the device address of the
- *  static array (with that device current).  Make that first call before any
- *  stream capture begins.
+ *  static array (with that device current), and so does the first call after
+ *  the device's CUDA context has been replaced (a device reset invalidates
+ *  the address; the library notices the new context and looks it up again).
+ *  Make that first call before any stream capture begins.
+ *
+ *  Work lists: the band-tile and global-row work lists are written into the
+ *  array by a small kernel on `stream` from values passed as kernel
+ *  parameters; no host buffer is copied and the call does not wait for the
+ *  stream.
  *
  *  Sharing: every call uses the same array, which keeps what the last call
  *  left there.  Each call writes every scratch byte it later reads, so nothing

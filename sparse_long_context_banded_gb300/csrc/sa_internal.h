@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "sa.h"
@@ -24,9 +25,7 @@ struct Slot {
 // coordinates, `rows` rows each) of head bh in residue class `slot`.  For query
 // tile u the key tiles k_lo[u]..k_hi[u] (inclusive, `key_tile` keys each)
 // intersect the band; flags bit u says whether any global key falls inside
-// that query tile's band reach (so the global tile must drop duplicates), and
-// bit 2 + u whether any of the tile's rows is a global row (whose output the
-// global-row pass writes: the band kernel leaves those rows alone).
+// that query tile's band reach (so the global tile must drop duplicates).
 struct BandItem {
   int32_t bh;
   int32_t slot;
@@ -123,6 +122,9 @@ std::vector<int32_t> global_set(const int32_t *idx, int n);
 Schedule build_schedule(const Problem &p, const Tiling &t);
 int64_t pairs_of_head(int N, int half, int d, const std::vector<int32_t> &globals);
 int64_t pairs_chunked(int N, int memory, int chunk);
+// About `want` key chunks of the N keys, each a multiple of `align` long (at
+// most max_chunks): (chunk length, chunk count).
+std::pair<int, int> key_chunks(int N, int64_t want, int64_t align, int64_t max_chunks);
 
 // Sets the thread-local message that sa_last_error() returns; returns s.
 sa_status record_error(sa_status s, const char *message);

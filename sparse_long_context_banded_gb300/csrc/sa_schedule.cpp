@@ -107,6 +107,13 @@ int64_t pairs_chunked(int N, int memory, int chunk) {
   return n;
 }
 
+std::pair<int, int> key_chunks(int N, int64_t want, int64_t align, int64_t max_chunks) {
+  want = std::max<int64_t>(1, std::min(want, max_chunks));
+  const int64_t per = (N + want - 1) / want;
+  const int64_t len = ((per + align - 1) / align) * align;
+  return std::pair<int, int>((int)len, (int)((N + len - 1) / len));
+}
+
 Schedule build_schedule(const Problem &p, const Tiling &t) {
   Schedule s;
   const int half = std::min(p.half, p.N);  // a wider band changes nothing
@@ -168,12 +175,13 @@ Schedule build_schedule(const Problem &p, const Tiling &t) {
             work += it.k_hi[u] - it.k_lo[u] + 1;
             s.band_tile_pairs += it.k_hi[u] - it.k_lo[u] + 1;
             // does a global key of this class fall inside the band reach?
-            // does a global row fall inside the tile?
             for (int32_t g : p.globals) {
               if ((g - r) % d != 0) continue;
               const int64_t tg = (g - r) / d;
-              if (tg >= reach_lo && tg <= reach_hi) it.flags |= 1 << u;
-              if (tg >= row_lo && tg <= row_hi) it.flags |= 4 << u;
+              if (tg >= reach_lo && tg <= reach_hi) {
+                it.flags |= 1 << u;
+                break;
+              }
             }
           }
           if (it.k_hi[0] >= it.k_lo[0] || it.k_hi[1] >= it.k_lo[1])  // not all memory rows
@@ -214,12 +222,7 @@ Schedule build_schedule(const Problem &p, const Tiling &t) {
     s.g_alt = t.q_tiles == 2 && n_g <= t.rows;
     s.g_packed = s.g_alt && 2 * n_g <= t.rows;
     const bool fused = t.fuse_global && t.sms > 1 && n_groups == 1;
-    auto chunk_of = [&](int64_t want, int64_t align) {
-      want = std::max<int64_t>(1, std::min(want, max_tiles));
-      const int64_t per = (p.N + want - 1) / want;
-      const int64_t len = ((per + align - 1) / align) * align;
-      return std::pair<int, int>((int)len, (int)((p.N + len - 1) / len));
-    };
+    auto chunk_of = [&](int64_t want, int64_t align) { return key_chunks(p.N, want, align, max_tiles); };
     if (!fused) {
       int64_t want = (t.target_ctas + bh * g_items - 1) / (bh * g_items);
       std::tie(s.chunk_len, s.n_chunks) = chunk_of(want, t.key_tile);

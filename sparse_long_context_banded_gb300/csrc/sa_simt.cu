@@ -270,7 +270,8 @@ template <typename T>
 __global__ void merge_kernel(DevProblem p) {
   // One block per (global row, head), one thread per output column.  Partial x
   // is row g + 64 (x % part_sub) of set x / part_sub.  The odd set of a chunk
-  // holding a single key tile was never written (g_alt), and a partial that
+  // holding a single key tile was never written (g_alt: the chunk's second
+  // query tile had no key tile to take), and a partial that
   // saw no key has max -inf and sum 0: both get weight 0.  Each partial's
   // (max, sum) pair is read once, as one 8-byte load; then every thread sums
   // its column over the partials, sixteen independent loads at a time (a

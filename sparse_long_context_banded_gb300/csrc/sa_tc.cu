@@ -371,19 +371,6 @@ __host__ __device__ constexpr uint32_t idesc_mma(int M, int N, bool b_mn_major, 
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Whether position pos is in the sorted global set (binary search).
-__device__ __forceinline__ bool is_global_position(const DevProblem &p, int64_t pos) {
-  int lo = 0, hi = p.n_g;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (p.globals[mid] < pos)
-      lo = mid + 1;
-    else
-      hi = mid;
-  }
-  return lo < p.n_g && p.globals[lo] == pos;
-}
-
 // Key tiles a global-row item keeps in flight to L2 ahead of its loads.
 constexpr int kGlobalAhead = 6;
 
@@ -865,9 +852,7 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
       bool ok = true;
       // output tile staged in each buffer: map index, first row, head
       int out_ls[C::kQBufs], out_row[C::kQBufs], out_bh[C::kQBufs];
-      bool out_direct[C::kQBufs];  // the tile holds global rows: its rows were stored one by one
       auto store_staged = [&](uint32_t b) {
-        if (out_direct[b]) return;
         for (int h = 0; h < C::kHalves; ++h)
           tma_store_3d(&P.maps.o[out_ls[b]], s_q0 + b * C::kQBytes + h * (kRows * 128),
                        C::kHalfCols * h, out_row[b], out_bh[b]);  // rows past the class end are clipped
@@ -922,7 +907,6 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
             out_ls[b] = w.slot - P.slot_base;
             out_row[b] = (w.q_tile + u) * kRows;
             out_bh[b] = w.bh;
-            out_direct[b] = ((w.flags >> (2 + u)) & 1) != 0;
           }
           mbar_expect_tx(B.q_full + 8 * b, C::kQBytes);
           if (GLOBAL && p.g_packed) {
@@ -1402,13 +1386,6 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
         // back to the Q producer once the store has read it
         uint8_t *stage = smem + qb * C::kQBytes;
         const float inv = rcp_approx(l_run);
-        // A tile holding global rows is not staged: each thread stores its own
-        // row, unless it is a global row (the global-row pass writes those,
-        // possibly while this kernel still runs) or past the class end.
-        const bool direct = ((w.flags >> (2 + u)) & 1) != 0;
-        const int64_t pos_q = (int64_t)w.r + (int64_t)w.d * t_q;
-        const bool mine = t_q < w.len && !(direct && is_global_position(p, pos_q));
-        uint8_t *grow = static_cast<uint8_t *>(p.out) + ((int64_t)w.bh * p.N + pos_q) * D * C::kElem;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -1425,10 +1402,7 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
                   __uint_as_float(r[q4 * 4 + 0]) * inv, __uint_as_float(r[q4 * 4 + 1]) * inv,
                   __uint_as_float(r[q4 * 4 + 2]) * inv, __uint_as_float(r[q4 * 4 + 3]) * inv);
               const int phys = (chunk0 + q4) ^ (row & 7);
-              if (!direct)
-                *reinterpret_cast<float4 *>(rowp + phys * 16) = v;
-              else if (mine)
-                *reinterpret_cast<float4 *>(grow + (c * 32 + q4 * 4) * 4) = v;
+              *reinterpret_cast<float4 *>(rowp + phys * 16) = v;
             }
           } else {
 #pragma unroll
@@ -1439,14 +1413,12 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
               v.z = pack_bf16(__uint_as_float(r[q4 * 8 + 4]) * inv, __uint_as_float(r[q4 * 8 + 5]) * inv);
               v.w = pack_bf16(__uint_as_float(r[q4 * 8 + 6]) * inv, __uint_as_float(r[q4 * 8 + 7]) * inv);
               const int phys = (chunk0 + q4) ^ (row & 7);
-              if (!direct)
-                *reinterpret_cast<uint4 *>(rowp + phys * 16) = v;
-              else if (mine)
-                *reinterpret_cast<uint4 *>(grow + (c * 32 + q4 * 8) * 2) = v;
+              *reinterpret_cast<uint4 *>(rowp + phys * 16) = v;
             }
           }
         }
-        if (p.lse && mine) {
+        if (p.lse && t_q < w.len) {
+          const int64_t pos_q = (int64_t)w.r + (int64_t)w.d * t_q;
           p.lse[(int64_t)w.bh * p.N + pos_q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
         }
         // the staged tile is handed to the Q producer, which stores it
@@ -1717,7 +1689,7 @@ cudaError_t launch_stalled_wait_check(int *err, uint32_t limit_us, cudaStream_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, bool precise, int BH, int ctas,
+cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, bool precise, int BH, int sms,
                              cudaStream_t s) {
   static thread_local tc::Params P;
   const bool tf = dt == SA_TF32;
@@ -1726,7 +1698,7 @@ cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, bool precise, int
   P.slot_base = 0;
   P.item_offset = 0;
   P.n_items = 0;
-  return launch_any(P, p.D, tf, precise, 0, std::min(p.n_gitems, std::max(ctas, 1)), s);
+  return launch_any(P, p.D, tf, precise, 0, std::min(p.n_gitems, std::max(sms, 1)), s);
 }
 
 }  // namespace sa

@@ -20,10 +20,10 @@ bool tc_supports(sa_dtype dt, int D);
 // Band tiles: one launch per group of at most 16 residue classes
 // (group_begin from the schedule).  host_slots mirrors p.slots on the host.
 // With g_ctas > 0 (a single group), the launch also runs the global-row items
-// on g_ctas CTAs of its own beside band_ctas band CTAs.  The rows of global
-// positions are not written by the band tiles (the merge of the global-row
-// partials writes them).  `precise`: P is split into two bf16 parts for the
-// P V product (bf16 inputs).
+// on g_ctas CTAs of its own beside band_ctas band CTAs.  The band tiles write
+// every row, global rows too; the merge of the global-row partials, enqueued
+// after them, overwrites those.  `precise`: P is split into two bf16 parts for
+// the P V product (bf16 inputs).
 cudaError_t launch_band_tc(const DevProblem &p, sa_dtype dt, bool precise, const Slot *host_slots,
                            int n_slots, const std::vector<int32_t> &group_begin, int BH, int sms,
                            int g_ctas, int band_ctas, cudaStream_t s);
@@ -33,8 +33,8 @@ cudaError_t launch_band_tc(const DevProblem &p, sa_dtype dt, bool precise, const
 cudaError_t launch_stalled_wait_check(int *err, uint32_t limit_us, cudaStream_t s);
 
 // Global rows against all keys, split over key chunks (partials for merge),
-// on at most `ctas` persistent CTAs.
-cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, bool precise, int BH, int ctas,
+// as a launch of its own on at most `sms` persistent CTAs.
+cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, bool precise, int BH, int sms,
                              cudaStream_t s);
 
 }  // namespace sa
