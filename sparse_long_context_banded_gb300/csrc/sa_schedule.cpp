@@ -232,15 +232,15 @@ Schedule build_schedule(const Problem &p, const Tiling &t) {
       //   band item: max over its query tiles of the band tiles, plus the
       //   global key tiles (64 keys: ~0.6 of a band tile);
       //   global item: its key tiles, alternate tiles going to the two query
-      //   tiles (measured at D = 128: a key tile of global rows costs ~1,900
-      //   SM cycles, a band unit ~4,600).
+      //   tiles (measured at D = 128: a key tile of global rows costs ~2,000
+      //   SM cycles, a band unit ~4,300).
       // The band items are spread over S - X CTAs, the global items over X.
       // The key chunks number X (or 2X), so that, with the items in head-major
       // order, every global CTA takes one chunk of each head in turn and the
       // global CTAs move through the heads together with the band CTAs (whose
       // items are in head order too): the keys and values they read were
       // loaded by the band tiles shortly before and come from L2.
-      const double kNarrow = 0.6, kGlobTile = 0.85, kMergePerPart = 0.15;
+      const double kNarrow = 0.6, kGlobTile = 0.93, kMergePerPart = 0.15;
       double band_total = 0.0, band_max = 0.0;
       for (const BandItem &it : s.band) {
         double c = 0.0;

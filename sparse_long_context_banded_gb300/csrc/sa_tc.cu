@@ -15,10 +15,16 @@
 //
 //   S = Q_u K_j^T (fp32 in TMEM; Q negated for a negative scale) -> mask (edge
 //   tiles only), running max / sum per row -> P = exp2(scale S - m) written
-//   back over S (bf16 pairs, or fp32 for tf32), in two halves -> O_u += P V_j
-//   (A operand from TMEM; the first half of the product starts once the first
-//   half of P is in place).  tf32 operands must be K-major, so for fp32 inputs
-//   the values arrive transposed (32-key chunks of D rows).
+//   back over S (bf16 pairs, or fp32 for tf32) -> O_u += P V_j (A operand from
+//   TMEM).  Band CTAs take each key tile as two 64-key sub-tiles whose S
+//   products alternate between the two halves of S_u's columns: the S of the
+//   next sub-tile is computed while the softmax works on the current one
+//   (its P sits in the other half), so a query tile's softmax does not wait
+//   for its own P V before the next scores exist.  Global-row CTAs take
+//   whole 128-key tiles, P written over S in two halves, the first half of
+//   P V starting once the first half of P is in place.  tf32 operands must be
+//   K-major, so for fp32 inputs the values arrive transposed (32-key chunks
+//   of D rows).
 //
 // In global mode the two query tiles are the gathered global rows and the key
 // tiles one chunk of all N keys; the CTA writes unnormalised partial outputs
@@ -494,7 +500,9 @@ __device__ __forceinline__ int seq_len(const Work &w, int u) {
 struct Bars {
   uint32_t slot_full, slot_empty;  // arrays of kSlots
   uint32_t q_full, q_empty;  // arrays of kQBufs
-  uint32_t s_full, p_half, p_full, o_final, mma_done, s_issued;  // arrays of 2
+  uint32_t s_full, p_half, p_full, o_final, mma_done, s_issued, pv_done;  // arrays of 2
+  // band sub-tiles: S complete and P written, per chain and S half ([2 u + half])
+  uint32_t s_sub, p_sub;
 };
 
 // ---------------------------------------------------------------------------
@@ -513,21 +521,25 @@ struct Bars {
 //   code has to stay small enough for the instruction caches of warps that
 //   run different roles on one sub-partition.
 
-// kKeys scores of this thread's row from TMEM, masked to -inf.
+// W (128 or 64) scores of this thread's row from TMEM, masked to -inf.
+template <int W>
 __device__ __forceinline__ void load_scores(uint32_t t_s, bool interval, int c_lo, int c_hi,
                                             const int32_t *globals, int g0, int t_q, int half,
-                                            bool dedup, float (&s)[kKeys]) {
+                                            bool dedup, float (&s)[W]) {
   {
-    uint32_t r[kKeys];
-    tmem_ld128(t_s, r);
+    uint32_t r[W];
+    if constexpr (W == 128)
+      tmem_ld128(t_s, r);
+    else
+      tmem_ld64(t_s, r);
 #pragma unroll
-    for (int x = 0; x < kKeys; ++x) s[x] = __uint_as_float(r[x]);
+    for (int x = 0; x < W; ++x) s[x] = __uint_as_float(r[x]);
   }
   // branch-free: a compare and a select per column (the bounds differ per row)
   if (interval) {
     const uint32_t span = (uint32_t)(c_hi - c_lo);
 #pragma unroll
-    for (int x = 0; x < kKeys; ++x) {
+    for (int x = 0; x < W; ++x) {
       const bool keep = (uint32_t)(x - c_lo) <= span;  // c_lo <= x <= c_hi
       s[x] = keep ? s[x] : -INFINITY;
     }
@@ -563,7 +575,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
   constexpr int W = kKeys;
   const float scl = scale;
   float s[W];
-  load_scores(t_s, interval, c_lo, c_hi, globals, g0, t_q, half, dedup, s);
+  load_scores<W>(t_s, interval, c_lo, c_hi, globals, g0, t_q, half, dedup, s);
   // row maximum: eight chains of three-input max
   float mx[8];
 #pragma unroll
@@ -655,6 +667,106 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
   const float2 s4 = __fadd2_rn(s01, s23);
   l_run = (need ? l_run * alpha : l_run) + (s4.x + s4.y);
   m_run = m_new;
+}
+
+// One 64-key sub-tile of a band item for one query row (this thread's TMEM
+// lane).  The scores sit in one half of the tile's S columns (t_s .. t_s+63);
+// P = 2^(scale*S - m) is written over the first columns of that half (bf16
+// pairs in 32 columns, the low parts of split P in the next 32; tf32 in all
+// 64), where only this sub-tile's P V reads it, so the S product of the
+// sub-tile after next -- the other half holds the next one -- can run while
+// this P is computed.  Running maximum and sum as in softmax_tile.  O is
+// rescaled when the reference maximum moves, after the previous sub-tile's
+// P V has completed: its commit is phase `pv_parity` of `pv_done` (the P V
+// before that one completed before this sub-tile's S, which follows it in
+// issue order, so the barrier is at most one phase behind).  Returns false
+// if that wait gave up.
+template <int D, bool TF, bool PRECISE>
+__device__ __forceinline__ bool softmax_sub(uint32_t t_s, uint32_t t_o, float scale, bool interval,
+                                            int c_lo, int c_hi, const int32_t *globals, int g0,
+                                            int t_q, int half, bool dedup, uint32_t pv_done,
+                                            uint32_t pv_parity, volatile int *abort_flag,
+                                            int *err, float &m_run, float &l_run) {
+  constexpr int W = kKeys / 2;
+  const float scl = scale;
+  float s[W];
+  load_scores<W>(t_s, interval, c_lo, c_hi, globals, g0, t_q, half, dedup, s);
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+  for (int x = 16; x < W; x += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[x + 2 * i], s[x + 2 * i + 1]);
+  const float mt =
+      max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * scl;
+  const bool need = mt > m_run + 8.f;
+  const float m_new = need ? mt : m_run;
+  const float alpha = need ? ex2(m_run - m_new) : 1.f;
+  const bool rescale = need && m_run != -INFINITY;  // O holds earlier sub-tiles of this row
+  const float neg = (m_new == -INFINITY) ? 0.f : -m_new;
+  const float2 scl2 = make_float2(scl, scl), neg2 = make_float2(neg, neg);
+  float2 sum2[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
+  if constexpr (PRECISE) {
+    static_assert(!TF, "split P is for bf16 inputs");
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq) {
+      uint32_t ph[16], pl[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int i = qq * 16 + j;
+        const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
+        const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
+        sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
+        ph[j] = pack_bf16(e.x, e.y);
+        pl[j] = pack_bf16_residual(e.x, e.y, ph[j]);
+      }
+      tmem_st16(t_s + qq * 16, ph);
+      tmem_st16(t_s + 32 + qq * 16, pl);
+    }
+  } else {
+    constexpr int kWords = TF ? W : W / 2;
+    uint32_t pr[kWords];
+#pragma unroll
+    for (int i = 0; i < W / 2; ++i) {
+      const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
+      const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
+      sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
+      if constexpr (TF) {
+        pr[2 * i] = __float_as_uint(e.x);
+        pr[2 * i + 1] = __float_as_uint(e.y);
+      } else {
+        pr[i] = pack_bf16(e.x, e.y);
+      }
+    }
+    if constexpr (TF)
+      tmem_st64(t_s, pr);
+    else
+      tmem_st32(t_s, pr);
+  }
+  bool ok = true;
+  if (__any_sync(0xffffffffu, rescale)) {
+    ok = __all_sync(0xffffffffu, wait_bar(pv_done, pv_parity, abort_flag, err));
+    if (ok) {
+      tc_fence_after();
+      const float a = rescale ? alpha : 1.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t r[16];
+        tmem_ld16(t_o + c * 16, r);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * a);
+        tmem_st16(t_o + c * 16, r);
+      }
+    }
+  }
+  const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+  const float2 s4 = __fadd2_rn(s01, s23);
+  l_run = (need ? l_run * alpha : l_run) + (s4.x + s4.y);
+  m_run = m_new;
+  return ok;
 }
 
 // Global rows packed twice into a query tile (at most 64 of them): the row
@@ -782,7 +894,7 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
   const uint32_t s_q0 = smem_u32(smem);
   const uint32_t s_slots = s_q0 + NQ * C::kQBytes;
   uint8_t *aux = smem + C::kRegion;
-  constexpr int kBars = 2 * C::kMaxSlots + 2 * C::kQBufs + 12;
+  constexpr int kBars = 2 * C::kMaxSlots + 2 * C::kQBufs + 22;
   uint64_t *bar_mem = reinterpret_cast<uint64_t *>(aux);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(aux + 8 * kBars);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(aux + 8 * kBars + 4);
@@ -799,6 +911,9 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
   B.o_final = B.p_full + 16;         // [2]
   B.mma_done = B.o_final + 16;       // [2]
   B.s_issued = B.mma_done + 16;      // [2]
+  B.pv_done = B.s_issued + 16;       // [2]
+  B.s_sub = B.pv_done + 16;          // [4]
+  B.p_sub = B.s_sub + 32;            // [4]
 
   const int tid = threadIdx.x;
   if (s_q0 & 1023u) {  // 128-byte-swizzled tiles need 1024-byte alignment
@@ -825,6 +940,11 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
       mbar_init(B.o_final + 8 * u, 1);
       mbar_init(B.mma_done + 8 * u, 1);
       mbar_init(B.s_issued + 8 * u, 1);
+      mbar_init(B.pv_done + 8 * u, 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(B.s_sub + 8 * (2 * u + h), 1);
+        mbar_init(B.p_sub + 8 * (2 * u + h), 4);
+      }
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1128,9 +1248,144 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
           base += 2u * (uint32_t)(u ? w.n_cnt[1] : w.n_cnt[0]);
         }
       }
+      if constexpr (!GLOBAL) {
+        // Band items in 64-key sub-tiles.  Sub-tile j of this chain (counted
+        // over all its items) has its S in the half (j & 1) of S_u's columns
+        // and its P over the first columns of that half, so the issue order
+        //   S(0), S(1), PV(0), S(2), PV(1), S(3), ...
+        // lets S(j + 1) overwrite the half of sub-tile j - 1 right after
+        // PV(j - 1) in issue order (MMAs of one thread execute in order),
+        // without waiting for P(j): the S product of the next sub-tile runs
+        // while the softmax works on this one.  The key tile of a position is
+        // read by its two sub-tiles (a global tile: one), the value tile by
+        // their P V products; both slots are released by a commit after the
+        // last MMA that reads them, or by a plain arrive, after the tile has
+        // landed, at a position this query tile does not reach.  At the end of
+        // an item, and before a position the tile does not reach, the pending
+        // P V is issued at once.
+        const uint32_t kIdescSh = idesc_mma(kRows, kKeys / 2, false, TF) | neg_a;
+        uint32_t pv = 0, jq = 0, sc = 0;  // sc: S products issued (sub-tiles)
+        int k_slot = 0, k_par = 0;
+        bool ok = true;
+        for (int item = item0; item < n_items && ok; item += stride) {
+          const Work w = make_work<GLOBAL>(P, item);
+          const bool act = u ? w.active[1] : w.active[0];
+          const uint32_t jt = jq + ((u == 1 && w.active[0]) ? 1u : 0u);
+          jq += (uint32_t)w.active[0] + (uint32_t)w.active[1];
+          const uint32_t qb = jt % NQ;
+          const uint64_t dq = sw128_desc(s_q0 + qb * C::kQBytes, 16, 1024);
+          if (act) {
+            ok = __all_sync(0xffffffffu, wait_bar(B.q_full + 8 * qb, (jt / NQ) & 1u, abort_flag, p.err));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          const int n_tiles = w.nb + w.ng;
+          const int a_u = (u ? w.n_lo[1] : w.n_lo[0]) - w.lo;
+          const int b_u = a_u + (u ? w.n_cnt[1] : w.n_cnt[0]);
+          // the sub-tile whose P V is still to be issued
+          bool pd = false, pd_glob = false, pd_last = false;
+          int pd_h = 0, pd_vslot = 0, pd_vpar = 0;
+          uint32_t pd_col = 0;
+          int pv_item = 0;
+          // Sub-tile j's barriers are those of its S half (j & 1), in their
+          // use (j >> 1): a waiter is never two phases behind, as sub-tile
+          // j + 2 cannot start before this sub-tile's P V is issued.
+          auto issue_pv = [&]() -> bool {
+            bool good = __all_sync(0xffffffffu, wait_bar(B.p_sub + 8 * (2 * u + (pv & 1u)), (pv >> 1) & 1u,
+                                                         abort_flag, p.err));
+            // the value tile: waited for by its first P V
+            if (good && pd_h == 0)
+              good = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * pd_vslot, pd_vpar, abort_flag, p.err));
+            if (!good) return false;
+            tc_fence_after();
+            const uint64_t off = (uint64_t)((pd_vslot * C::kSlotBytes) >> 4);
+            const uint32_t first = pv_item == 0 ? 0u : 1u;
+            const uint32_t a = d_s + pd_col;
+            const uint64_t dv = pd_glob ? dv_glob : dv_band;
+            const int k0 = pd_glob ? 0 : pd_h * kPvHalf;  // first K step in the value tile
+#pragma unroll
+            for (int kk = 0; kk < kPvHalf; ++kk)
+              mma_ts_warp<TF>(d_o, a + kk * 8, dv + off + v_step(k0 + kk), kIdescPV, kk > 0 ? 1u : first);
+            if constexpr (PRECISE) {
+              // the low parts of split P, 32 columns after the high parts
+#pragma unroll
+              for (int kk = 0; kk < kPvHalf; ++kk)
+                mma_ts_warp<TF>(d_o, a + 32 + kk * 8, dv + off + v_step(k0 + kk), kIdescPV, 1u);
+            }
+            ++pv;
+            ++pv_item;
+            mma_commit_warp(B.pv_done + 8 * u);
+            if (pd_last) mma_commit_warp(B.slot_empty + 8 * pd_vslot);
+            pd = false;
+            return true;
+          };
+          for (int i = 0; i < n_tiles && ok; ++i) {
+            const bool gc = is_global_pos(w, i);
+            const int ib = band_index(w, i);
+            const bool reads = act && (gc || (ib >= a_u && ib < b_u));
+            int v_slot = k_slot + 1, v_par = k_par;  // the value tile follows the key tile
+            if (v_slot == NS) {
+              v_slot = 0;
+              v_par ^= 1;
+            }
+            ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * k_slot, k_par, abort_flag, p.err));
+            if (!ok) break;
+            if (reads) {
+              tc_fence_after();
+              const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
+              const int n_sub = gc ? 1 : 2;
+              for (int h = 0; h < n_sub && ok; ++h) {
+                const uint32_t col = (sc & 1u) * 64u;
+                // K steps of 32 bytes of a row: four per 128-byte swizzled row
+                // chunk, then on to the next chunk; sub-tile h starts 64 key
+                // rows into each chunk of a band tile
+                if (!gc) {
+#pragma unroll
+                  for (int kk = 0; kk < D / C::kMmaK; ++kk)
+                    mma_ss_warp<TF>(d_s + col, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                                    dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32 + h * (kKeys / 2) * 128) >> 4),
+                                    kIdescSh, kk > 0);
+                } else {
+#pragma unroll
+                  for (int kk = 0; kk < D / C::kMmaK; ++kk)
+                    mma_ss_warp<TF>(d_s + col, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                                    dk + (((kk >> 2) * (kGKeys * 128) + (kk & 3) * 32) >> 4), kIdescSg, kk > 0);
+                }
+                mma_commit_warp(B.s_sub + 8 * (2 * u + (sc & 1u)));
+                if (h == n_sub - 1) mma_commit_warp(B.slot_empty + 8 * k_slot);
+                ++sc;
+                if (pd) ok = issue_pv();
+                pd = true;
+                pd_glob = gc;
+                pd_last = h == n_sub - 1;
+                pd_h = h;
+                pd_col = col;
+                pd_vslot = v_slot;
+                pd_vpar = v_par;
+              }
+            } else {
+              mbar_arrive_warp(B.slot_empty + 8 * k_slot);
+              if (pd) ok = issue_pv();
+              if (ok) ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * v_slot, v_par, abort_flag, p.err));
+              if (!ok) break;
+              mbar_arrive_warp(B.slot_empty + 8 * v_slot);
+            }
+            k_slot += 2;  // advance by two loads (K_i, V_i)
+            if (k_slot >= NS) {
+              k_slot -= NS;
+              k_par ^= 1;
+            }
+          }
+          if (ok && pd) ok = issue_pv();
+          // O_u is final once every P V of the item has completed (the last
+          // one may have been issued before a position this tile does not
+          // reach)
+          if (ok && pv_item > 0) mma_commit_warp(B.o_final + 8 * u);
+        }
+      } else {
       uint32_t pv = 0, jq = 0, g = 0;  // jq: query tiles of earlier items
       int k_slot = 0, k_par = 0;  // ring position and phase of the next K load
-      bool ok = !(GLOBAL && p.g_alt);  // (the alternating issuer above has run instead)
+      bool ok = !p.g_alt;  // (the alternating issuer above has run instead)
       for (int item = item0; item < n_items && ok; item += stride) {
         const Work w = make_work<GLOBAL>(P, item);
         const bool act = u ? w.active[1] : w.active[0];
@@ -1259,6 +1514,7 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
           }
         }
       }
+      }
       // everything this thread issued has completed before TMEM is released
       mma_commit_warp(B.mma_done + 8 * u);
       __syncwarp();
@@ -1332,6 +1588,43 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
       const bool packed = GLOBAL && p.g_packed;
       const int sub = row >> 6;
       float m_run = -INFINITY, l_run = 0.f;
+      if constexpr (!GLOBAL) {
+        // 64-key sub-tiles (a global tile is one), S in alternate halves of
+        // S_u's columns, as the issuer computes them
+        for (int i = 0; i < n && ok; ++i) {
+          const int pos = seq_pos_s(w, nlo_u, ncnt_u, i);
+          const bool gt = is_global_pos(w, pos);
+          const int n_sub = gt ? 1 : 2;
+          for (int h = 0; h < n_sub; ++h) {
+            bool interval = true;
+            int c_lo = 0, c_hi, g0 = 0;
+            if (!gt) {
+              const int kb = (w.lo + band_index(w, pos)) * kKeys + h * (kKeys / 2);
+              interval = !(lo_last <= kb && hi_first >= kb + kKeys / 2 - 1);
+              c_lo = r_lo - kb;
+              c_hi = r_hi - kb;
+            } else {
+              g0 = global_index(w, pos) * kGKeys;
+              c_hi = min(p.n_g - 1 - g0, kGKeys - 1);
+            }
+            const bool dedup = gt && ((w.flags >> u) & 1);
+            const uint32_t col = (scnt & 1u) * 64u;
+            const uint32_t sb = 2 * u + (scnt & 1u);  // this sub-tile's S half
+            ok = __all_sync(0xffffffffu, wait_bar(B.s_sub + 8 * sb, (scnt >> 1) & 1u, abort_flag, p.err));
+            if (!ok) break;
+            tc_fence_after();
+            ok = softmax_sub<D, TF, PRECISE>(t_s + col, t_o, sl, interval, c_lo, c_hi, g_list, g0, t_q,
+                                             half, dedup, B.pv_done + 8 * u, (scnt - 1u) & 1u,
+                                             abort_flag, p.err, m_run, l_run);
+            ++scnt;
+            if (!ok) break;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.p_sub + 8 * sb);
+          }
+        }
+      } else
       for (int i = 0; i < n && ok; ++i) {
         // global rows in one query tile: tile u takes the key tiles u, u+2, ...
         const int pos = (GLOBAL && p.g_alt) ? 2 * i + u : seq_pos_s(w, nlo_u, ncnt_u, i);
