@@ -669,6 +669,24 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, float s
   m_run = m_new;
 }
 
+// P of a 64-key sub-tile that this thread's row does not score: zeros, so
+// that the sub-tile's P V product adds nothing to the row.
+template <bool TF, bool PRECISE>
+__device__ __forceinline__ void zero_p_sub(uint32_t t_s) {
+  if constexpr (TF) {
+    uint32_t z[64];
+#pragma unroll
+    for (int x = 0; x < 64; ++x) z[x] = 0u;
+    tmem_st64(t_s, z);
+  } else {
+    uint32_t z[32];
+#pragma unroll
+    for (int x = 0; x < 32; ++x) z[x] = 0u;
+    tmem_st32(t_s, z);
+    if constexpr (PRECISE) tmem_st32(t_s + 32, z);
+  }
+}
+
 // One 64-key sub-tile of a band item for one query row (this thread's TMEM
 // lane).  The scores sit in one half of the tile's S columns (t_s .. t_s+63);
 // P = 2^(scale*S - m) is written over the first columns of that half (bf16
@@ -767,114 +785,6 @@ __device__ __forceinline__ bool softmax_sub(uint32_t t_s, uint32_t t_o, float sc
   l_run = (need ? l_run * alpha : l_run) + (s4.x + s4.y);
   m_run = m_new;
   return ok;
-}
-
-// Global rows packed twice into a query tile (at most 64 of them): the row
-// of this thread holds one copy of global row (row & 63) and scores only the
-// keys of its half `sub` of the key tile (S columns 64 sub .. 64 sub + 63; the
-// other copy scores the other half), keeping a running maximum and sum of its
-// own.  P of those keys goes to the half's P columns and zeros to the other
-// half's, so that the full-tile P V product adds exactly this half's keys into
-// the row's O; the two copies leave two partials of the global row.  Keys
-// past column c_hi of the half (the end of the chunk) are masked.
-template <int D, bool TF, bool PRECISE>
-__device__ __forceinline__ void softmax_packed(uint32_t t_s, uint32_t t_o, float scale, int sub,
-                                               int c_hi, float &m_run, float &l_run) {
-  constexpr int W = kKeys / 2;
-  constexpr int kWords = TF ? W : W / 2;  // P columns of one half
-  const float scl = scale;
-  float s[W];
-  {
-    uint32_t r[W];
-    tmem_ld64(t_s + sub * W, r);
-#pragma unroll
-    for (int x = 0; x < W; ++x) s[x] = __uint_as_float(r[x]);
-  }
-  {
-    // the other half's P columns (and their low parts) are zero for this row
-    uint32_t z[kWords];
-#pragma unroll
-    for (int x = 0; x < kWords; ++x) z[x] = 0u;
-    if constexpr (TF) {
-      tmem_st64(t_s + (1 - sub) * kWords, z);
-    } else {
-      tmem_st32(t_s + (1 - sub) * kWords, z);
-      if constexpr (PRECISE) tmem_st32(t_s + 64 + (1 - sub) * kWords, z);
-    }
-  }
-  if (c_hi < W - 1) {
-#pragma unroll
-    for (int x = 0; x < W; ++x) s[x] = x <= c_hi ? s[x] : -INFINITY;
-  }
-  float mx[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-  for (int x = 16; x < W; x += 16)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[x + 2 * i], s[x + 2 * i + 1]);
-  const float mt =
-      max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * scl;
-  const bool need = mt > m_run + 8.f;
-  const float m_new = need ? mt : m_run;
-  const float alpha = need ? ex2(m_run - m_new) : 1.f;
-  const bool rescale = need && m_run != -INFINITY;
-  if (__any_sync(0xffffffffu, rescale)) {
-    const float a = rescale ? alpha : 1.f;
-#pragma unroll 1
-    for (int c = 0; c < D / 16; ++c) {
-      uint32_t r[16];
-      tmem_ld16(t_o + c * 16, r);
-#pragma unroll
-      for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * a);
-      tmem_st16(t_o + c * 16, r);
-    }
-  }
-  const float neg = (m_new == -INFINITY) ? 0.f : -m_new;
-  const float2 scl2 = make_float2(scl, scl), neg2 = make_float2(neg, neg);
-  float2 sum2[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
-  if constexpr (PRECISE) {
-    static_assert(!TF, "split P is for bf16 inputs");
-#pragma unroll
-    for (int qq = 0; qq < 2; ++qq) {
-      uint32_t ph[16], pl[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int i = qq * 16 + j;
-        const float2 arg = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scl2, neg2);
-        const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
-        sum2[i & 3] = __fadd2_rn(sum2[i & 3], e);
-        ph[j] = pack_bf16(e.x, e.y);
-        pl[j] = pack_bf16_residual(e.x, e.y, ph[j]);
-      }
-      tmem_st16(t_s + sub * kWords + qq * 16, ph);
-      tmem_st16(t_s + 64 + sub * kWords + qq * 16, pl);
-    }
-  } else {
-    uint32_t pr[kWords];
-#pragma unroll
-    for (int j = 0; j < W / 2; ++j) {
-      const float2 arg = __ffma2_rn(make_float2(s[2 * j], s[2 * j + 1]), scl2, neg2);
-      const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
-      sum2[j & 3] = __fadd2_rn(sum2[j & 3], e);
-      if constexpr (TF) {
-        pr[2 * j] = __float_as_uint(e.x);
-        pr[2 * j + 1] = __float_as_uint(e.y);
-      } else {
-        pr[j] = pack_bf16(e.x, e.y);
-      }
-    }
-    if constexpr (TF)
-      tmem_st64(t_s + sub * kWords, pr);
-    else
-      tmem_st32(t_s + sub * kWords, pr);
-  }
-  const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
-  const float2 s4 = __fadd2_rn(s01, s23);
-  l_run = (need ? l_run * alpha : l_run) + (s4.x + s4.y);
-  m_run = m_new;
 }
 
 template <int D, bool GLOBAL, bool TF, bool PRECISE>
@@ -1169,14 +1079,16 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
       if (GLOBAL && p.g_alt) {
         // Global rows in one query tile: chain u reads only the key tiles u,
         // u+2, ... of each item, so this issuer visits only those -- no
-        // ping-pong hand-off, as the chains share no tile.  Chain u's loads
-        // cycle through its half of the ring (slots u NS/2 ..): the keys of
-        // its i-th tile are its load base + 2 i (values: + 1), and it alone
-        // waits on and releases those slots.
+        // hand-off, as the chains share no tile.  Chain u's loads cycle
+        // through its half of the ring (slots u NS/2 ..): the keys of its i-th
+        // tile are its load base + 2 i (values: + 1), and it alone waits on and
+        // releases those slots.  Each key tile is taken as two 64-key
+        // sub-tiles in the order of the band items (S of sub-tile j in the half
+        // j & 1 of S_u's columns, S(j + 1) issued right after PV(j - 1)).
         const int nsc = NS / 2;
-        uint32_t pv = 0, jq = 0, base = 0;
+        const uint32_t kIdescSh = idesc_mma(kRows, kKeys / 2, false, TF) | neg_a;
+        uint32_t pv = 0, jq = 0, base = 0, sc = 0;
         bool ok = true;
-        const bool one_piece = p.g_packed;  // packed rows: P arrives in one piece
         for (int item = item0; item < n_items && ok; item += stride) {
           const Work w = make_work<GLOBAL>(P, item);
           const bool act = u ? w.active[1] : w.active[0];
@@ -1189,62 +1101,67 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
           ok = __all_sync(0xffffffffu, wait_bar(B.q_full + 8 * qb, (jt / NQ) & 1u, abort_flag, p.err));
           if (!ok) break;
           tc_fence_after();
-          for (int i = 0; i <= n_u && ok; ++i) {
-            if (i > 0) {
-              // P V of this chain's previous tile
-              const uint32_t nv = base + 2u * (uint32_t)(i - 1) + 1u;
-              const int v_slot = u * nsc + (int)(nv % (uint32_t)nsc);
-              const uint32_t v_par = (nv / (uint32_t)nsc) & 1u;
-              ok = __all_sync(0xffffffffu, wait_bar(one_piece ? p_full : B.p_half + 8 * u, pv & 1u, abort_flag, p.err));
-              if (ok) ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * v_slot, v_par, abort_flag, p.err));
-              if (!ok) break;
-              tc_fence_after();
-              const uint64_t off = (uint64_t)((v_slot * C::kSlotBytes) >> 4);
-              const uint32_t first = i == 1 ? 0u : 1u;
-              if (!one_piece) {
+          bool pd = false;
+          int pd_h = 0, pd_vslot = 0;
+          uint32_t pd_vpar = 0, pd_col = 0;
+          int pv_item = 0;
+          auto issue_pv = [&]() -> bool {
+            bool good = __all_sync(0xffffffffu, wait_bar(B.p_sub + 8 * (2 * u + (pv & 1u)), (pv >> 1) & 1u,
+                                                         abort_flag, p.err));
+            if (good && pd_h == 0)
+              good = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * pd_vslot, pd_vpar, abort_flag, p.err));
+            if (!good) return false;
+            tc_fence_after();
+            const uint64_t off = (uint64_t)((pd_vslot * C::kSlotBytes) >> 4);
+            const uint32_t first = pv_item == 0 ? 0u : 1u;
+            const uint32_t a = d_s + pd_col;
 #pragma unroll
-                for (int kk = 0; kk < kPvHalf; ++kk)
-                  mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_band + off + v_step(kk), kIdescPV,
-                                  kk > 0 ? 1u : first);
-                if constexpr (PRECISE) {
+            for (int kk = 0; kk < kPvHalf; ++kk)
+              mma_ts_warp<TF>(d_o, a + kk * 8, dv_band + off + v_step(pd_h * kPvHalf + kk), kIdescPV,
+                              kk > 0 ? 1u : first);
+            if constexpr (PRECISE) {
 #pragma unroll
-                  for (int kk = 0; kk < kPvHalf; ++kk)
-                    mma_ts_warp<TF>(d_o, d_s + 64 + kk * 8, dv_band + off + v_step(kk), kIdescPV, 1u);
-                }
-                ok = __all_sync(0xffffffffu, wait_bar(p_full, pv & 1u, abort_flag, p.err));
-                if (!ok) break;
-                tc_fence_after();
-              }
-#pragma unroll
-              for (int kk = one_piece ? 0 : kPvHalf; kk < 2 * kPvHalf; ++kk)
-                mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_band + off + v_step(kk), kIdescPV,
-                                kk > 0 ? 1u : first);
-              if constexpr (PRECISE) {
-#pragma unroll
-                for (int kk = one_piece ? 0 : kPvHalf; kk < 2 * kPvHalf; ++kk)
-                  mma_ts_warp<TF>(d_o, d_s + 64 + kk * 8, dv_band + off + v_step(kk), kIdescPV, 1u);
-              }
-              ++pv;
-              mma_commit_warp(B.slot_empty + 8 * v_slot);
-              if (i == n_u) mma_commit_warp(B.o_final + 8 * u);
+              for (int kk = 0; kk < kPvHalf; ++kk)
+                mma_ts_warp<TF>(d_o, a + 32 + kk * 8, dv_band + off + v_step(pd_h * kPvHalf + kk), kIdescPV, 1u);
             }
-            if (i < n_u) {
-              // S of this chain's next tile
-              const uint32_t nk = base + 2u * (uint32_t)i;
-              const int k_slot = u * nsc + (int)(nk % (uint32_t)nsc);
-              const uint32_t k_par = (nk / (uint32_t)nsc) & 1u;
-              ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * k_slot, k_par, abort_flag, p.err));
-              if (!ok) break;
-              tc_fence_after();
-              const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
+            ++pv;
+            ++pv_item;
+            mma_commit_warp(B.pv_done + 8 * u);
+            if (pd_h == 1) mma_commit_warp(B.slot_empty + 8 * pd_vslot);
+            pd = false;
+            return true;
+          };
+          for (int i = 0; i < n_u && ok; ++i) {
+            const uint32_t nk = base + 2u * (uint32_t)i;
+            const int k_slot = u * nsc + (int)(nk % (uint32_t)nsc);
+            const uint32_t k_par = (nk / (uint32_t)nsc) & 1u;
+            const uint32_t nv = nk + 1u;
+            const int v_slot = u * nsc + (int)(nv % (uint32_t)nsc);
+            const uint32_t v_par = (nv / (uint32_t)nsc) & 1u;
+            ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * k_slot, k_par, abort_flag, p.err));
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
+            for (int h = 0; h < 2 && ok; ++h) {
+              const uint32_t col = (sc & 1u) * 64u;
 #pragma unroll
               for (int kk = 0; kk < D / C::kMmaK; ++kk)
-                mma_ss_warp<TF>(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
-                                dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
-              mma_commit_warp(s_full);
-              mma_commit_warp(B.slot_empty + 8 * k_slot);
+                mma_ss_warp<TF>(d_s + col, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
+                                dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32 + h * (kKeys / 2) * 128) >> 4),
+                                kIdescSh, kk > 0);
+              mma_commit_warp(B.s_sub + 8 * (2 * u + (sc & 1u)));
+              if (h == 1) mma_commit_warp(B.slot_empty + 8 * k_slot);
+              ++sc;
+              if (pd) ok = issue_pv();
+              pd = true;
+              pd_h = h;
+              pd_col = col;
+              pd_vslot = v_slot;
+              pd_vpar = v_par;
             }
           }
+          if (ok && pd) ok = issue_pv();
+          if (ok && pv_item > 0) mma_commit_warp(B.o_final + 8 * u);
           base += 2u * (uint32_t)(u ? w.n_cnt[1] : w.n_cnt[0]);
         }
       }
@@ -1624,44 +1541,55 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
             if (lane == 0) mbar_arrive(B.p_sub + 8 * sb);
           }
         }
-      } else
-      for (int i = 0; i < n && ok; ++i) {
-        // global rows in one query tile: tile u takes the key tiles u, u+2, ...
-        const int pos = (GLOBAL && p.g_alt) ? 2 * i + u : seq_pos_s(w, nlo_u, ncnt_u, i);
-        const bool gt = is_global_pos(w, pos);
-        // the tile's masks are set up before its S is awaited
-        bool interval = true;
-        int c_lo = 0, c_hi, g0 = 0;
-        if (!gt) {
-          const int kb = GLOBAL ? (w.key0 + band_index(w, pos) * kKeys) : (w.lo + band_index(w, pos)) * kKeys;
-          if (GLOBAL) {
-            interval = kb + kKeys > w.key_end;
-            c_hi = w.key_end - 1 - kb;
-          } else {
-            interval = !(lo_last <= kb && hi_first >= kb + kKeys - 1);
-            c_lo = r_lo - kb;
-            c_hi = r_hi - kb;
+      } else if (p.g_alt) {
+        // Global rows in one query tile: chain u takes the key tiles u, u+2,
+        // ... as 64-key sub-tiles, as the issuer computes them.  A packed row
+        // scores only the sub-tiles of its key half (the other copy of the row
+        // scores the other half); for the other sub-tiles, and for keys past
+        // the end of the chunk, its P is zero.
+        for (int i = 0; i < n && ok; ++i) {
+          const int kb = w.key0 + (2 * i + u) * kKeys;
+          const int c_hi = w.key_end - 1 - kb;  // last key of the chunk, as a column of the tile
+          for (int h = 0; h < 2; ++h) {
+            const int c_hi_h = c_hi - h * (kKeys / 2);
+            const bool scores = (!packed || sub == h) && c_hi_h >= 0;  // warp-uniform
+            const uint32_t col = (scnt & 1u) * 64u;
+            const uint32_t sb = 2 * u + (scnt & 1u);
+            ok = __all_sync(0xffffffffu, wait_bar(B.s_sub + 8 * sb, (scnt >> 1) & 1u, abort_flag, p.err));
+            if (!ok) break;
+            tc_fence_after();
+            if (scores)
+              ok = softmax_sub<D, TF, PRECISE>(t_s + col, t_o, sl, c_hi_h < kKeys / 2 - 1, 0, c_hi_h, g_list,
+                                               0, 0, half, false, B.pv_done + 8 * u, (scnt - 1u) & 1u,
+                                               abort_flag, p.err, m_run, l_run);
+            else
+              zero_p_sub<TF, PRECISE>(t_s + col);
+            ++scnt;
+            if (!ok) break;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.p_sub + 8 * sb);
           }
-        } else {
-          // a global tile holds kGKeys gathered keys; the columns past them
-          // (and past the last global) are masked
-          g0 = global_index(w, pos) * kGKeys;
-          c_hi = min(p.n_g - 1 - g0, kGKeys - 1);
         }
-        const bool dedup = gt && ((w.flags >> u) & 1);
-        ok = __all_sync(0xffffffffu, wait_bar(B.s_full + 8 * u, scnt & 1u, abort_flag, p.err));
-        ++scnt;
-        if (!ok) break;
-        tc_fence_after();
-        if (packed)
-          softmax_packed<D, TF, PRECISE>(t_s, t_o, sl, sub, c_hi - sub * (kKeys / 2), m_run, l_run);
-        else
-          softmax_tile<D, TF, PRECISE>(t_s, t_o, sl, interval, c_lo, c_hi, g_list, g0, t_q, half,
-                                       dedup, gt, B.p_half + 8 * u, lane, m_run, l_run);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(B.p_full + 8 * u);
+      } else {
+        // more global rows than one query tile holds: each query tile takes
+        // every key tile of the chunk, whole (P in two halves)
+        for (int i = 0; i < n && ok; ++i) {
+          const int kb = w.key0 + i * kKeys;
+          const bool interval = kb + kKeys > w.key_end;
+          const int c_hi = w.key_end - 1 - kb;
+          ok = __all_sync(0xffffffffu, wait_bar(B.s_full + 8 * u, scnt & 1u, abort_flag, p.err));
+          ++scnt;
+          if (!ok) break;
+          tc_fence_after();
+          softmax_tile<D, TF, PRECISE>(t_s, t_o, sl, interval, 0, c_hi, g_list, 0, t_q, half, false,
+                                       false, B.p_half + 8 * u, lane, m_run, l_run);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(B.p_full + 8 * u);
+        }
       }
 
       // every thread of the warpgroup takes part in the same barriers, so the
