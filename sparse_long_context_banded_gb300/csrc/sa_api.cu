@@ -443,8 +443,10 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
       p.globals.back() - p.globals.front() + 1 == (int32_t)p.globals.size())
     dp.g_first = p.globals.front();
   dp.slots = sched->slots;
+  dp.n_slots = (int)hs.slots.size();
   dp.band = sched->band;
   dp.n_band = (int)hs.band.size();
+  dp.BH = B * H;
   dp.gitems = sched->global;
   dp.n_gitems = (int)hs.global.size();
   dp.n_chunks = hs.n_chunks;

@@ -34,8 +34,10 @@ struct DevProblem {
   // queries' source), k and v instead of gathered copies; -1 otherwise
   int g_first;
   const Slot *slots;
+  int n_slots;
   const BandItem *band;
   int n_band;
+  int BH;  // batch x heads
   const GlobalItem *gitems;
   int n_gitems;
   int n_chunks, chunk_len;

@@ -370,8 +370,10 @@ extern "C" sa_status sa_forward_noalloc(const void *q, const void *k, const void
   dp.n_g = n_g;
   dp.g_pad = L.g_pad;
   dp.slots = reinterpret_cast<const Slot *>(base + L.slots);
+  dp.n_slots = L.slot_off[H];
   dp.band = reinterpret_cast<const BandItem *>(base + L.band);
   dp.n_band = B * L.item_off[H];
+  dp.BH = B * H;
   dp.gitems = reinterpret_cast<const GlobalItem *>(base + L.global);
   dp.n_gitems = (int)(bh * L.n_chunks * L.g_items);
   dp.n_chunks = L.n_chunks;

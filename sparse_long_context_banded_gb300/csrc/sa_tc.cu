@@ -62,6 +62,13 @@
 #include "sa_tc.h"
 #include "sa_tmem_ops.h"
 
+#ifndef SA_DEBUG
+#define SA_DEBUG 0
+#endif
+#if SA_DEBUG
+#include "sa_debug.h"
+#endif
+
 namespace sa {
 namespace tc {
 
@@ -413,12 +420,42 @@ struct Work {
   int g_tile;    // global mode: pair of 128-row tiles of the gathered global rows
 };
 
+#if SA_DEBUG
+// Range checks of the work descriptions (SA_DEBUG builds): a band item's
+// residue class lies in the problem's classes and in this launch's window of
+// kMaxSlotsPerLaunch tensor maps, its head in [0, BH), its query tile and
+// every key-tile range it lists inside the class; a global-row item's head,
+// key chunk and tile of global rows inside the problem.
+__device__ __forceinline__ bool band_item_in_range(const BandItem &it, const Slot *slots, int n_slots,
+                                                   int slot_base, int BH) {
+  const int ls = it.slot - slot_base;
+  if (it.slot < 0 || it.slot >= n_slots || ls < 0 || ls >= kMaxSlotsPerLaunch) return false;
+  if (it.bh < 0 || it.bh >= BH) return false;
+  const Slot sl = slots[it.slot];
+  if (it.q_tile < 0 || (int64_t)it.q_tile * kRows >= sl.len) return false;
+  for (int u = 0; u < 2; ++u)
+    if (it.k_hi[u] >= it.k_lo[u] && (it.k_lo[u] < 0 || (int64_t)it.k_hi[u] * kKeys >= sl.len)) return false;
+  return true;
+}
+__device__ __forceinline__ bool global_item_in_range(const GlobalItem &it, const DevProblem &p) {
+  return it.bh >= 0 && it.bh < p.BH && it.chunk >= 0 && it.chunk < p.n_chunks && it.g_tile >= 0 &&
+         (int64_t)it.g_tile * 2 * kRows < p.g_pad;
+}
+#endif
+
 template <bool GLOBAL>
 __device__ __forceinline__ Work make_work(const Params &P, int item) {
   Work w{};
   const DevProblem &p = P.p;
   if (!GLOBAL) {
     const BandItem it = p.band[P.item_offset + item];
+#if SA_DEBUG
+    if (!band_item_in_range(it, p.slots, p.n_slots, P.slot_base, p.BH)) {
+      // no tiles and no rows: every role skips the item
+      if (p.err) atomicOr(p.err, kErrBadWork);
+      return w;
+    }
+#endif
     const Slot sl = p.slots[it.slot];
     w.bh = it.bh;
     w.slot = it.slot;
@@ -442,6 +479,12 @@ __device__ __forceinline__ Work make_work(const Params &P, int item) {
     w.ng = (p.n_g + kGKeys - 1) / kGKeys;
   } else {
     const GlobalItem it = p.gitems[item];
+#if SA_DEBUG
+    if (!global_item_in_range(it, p)) {
+      if (p.err) atomicOr(p.err, kErrBadWork);
+      return w;
+    }
+#endif
     w.bh = it.bh;
     w.chunk = it.chunk;
     w.g_tile = it.g_tile;
@@ -1923,3 +1966,47 @@ cudaError_t launch_global_tc(const DevProblem &p, sa_dtype dt, bool precise, int
 }
 
 }  // namespace sa
+
+#if SA_DEBUG
+namespace sa {
+namespace tc {
+namespace {
+__global__ void check_band_items_kernel(const BandItem *items, int n, const Slot *slots, int n_slots,
+                                        int slot_base, int BH, int *n_bad) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n && !band_item_in_range(items[i], slots, n_slots, slot_base, BH)) atomicAdd(n_bad, 1);
+}
+}  // namespace
+}  // namespace tc
+}  // namespace sa
+
+// The band-item range check of the SA_DEBUG kernels, run by itself on a
+// list of items (include/sa_debug.h).
+extern "C" sa_status sa_debug_check_band_items(const void *items, int n_items, const void *slots,
+                                               int n_slots, int slot_base, int BH, int *n_bad) {
+  using namespace sa;
+  if (!items || !slots || !n_bad || n_items < 0 || n_slots <= 0)
+    return record_error(SA_ERR_INVALID_ARG, "sa_debug_check_band_items: null pointer or bad count");
+  BandItem *d_items = nullptr;
+  Slot *d_slots = nullptr;
+  int *d_bad = nullptr;
+  cudaError_t e = cudaMalloc(&d_items, sizeof(BandItem) * (size_t)(n_items > 0 ? n_items : 1));
+  if (e == cudaSuccess) e = cudaMalloc(&d_slots, sizeof(Slot) * (size_t)n_slots);
+  if (e == cudaSuccess) e = cudaMalloc(&d_bad, sizeof(int));
+  if (e == cudaSuccess && n_items > 0)
+    e = cudaMemcpy(d_items, items, sizeof(BandItem) * (size_t)n_items, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(d_slots, slots, sizeof(Slot) * (size_t)n_slots, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(d_bad, 0, sizeof(int));
+  if (e == cudaSuccess && n_items > 0) {
+    tc::check_band_items_kernel<<<(n_items + 127) / 128, 128>>>(d_items, n_items, d_slots, n_slots,
+                                                                slot_base, BH, d_bad);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaMemcpy(n_bad, d_bad, sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFree(d_items);
+  cudaFree(d_slots);
+  cudaFree(d_bad);
+  if (e != cudaSuccess) return record_error(SA_ERR_CUDA, cudaGetErrorString(e));
+  return SA_OK;
+}
+#endif

@@ -90,6 +90,38 @@ def load(path: Optional[str] = None):
     return lib
 
 
+# the SA_DEBUG build's test entry point (include/sa_debug.h)
+DEBUG_SIGNATURES = {
+    "sa_debug_check_band_items": (_I, [_VP, _I, _VP, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
+}
+
+_lib_debug = None
+
+
+def library_path_debug() -> str:
+    return _build.LIBPATH_DEBUG
+
+
+def load_debug():
+    """Load the SA_DEBUG build (build it first with ``build.build(debug=True)``):
+    the same entry points with device-side range checks of every work
+    description, plus ``sa_debug_check_band_items``.  It is loaded beside the
+    release library, not in its place."""
+    global _lib_debug
+    if _lib_debug is not None:
+        return _lib_debug
+    p = library_path_debug()
+    if not os.path.exists(p):
+        raise RuntimeError(f"SA_DEBUG library not built: {p} is missing (run build.build(debug=True))")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in {**SIGNATURES, **DEBUG_SIGNATURES}.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib_debug = lib
+    return lib
+
+
 def _check(status: int):
     if status != SA_OK:
         raise SaError(status, load().sa_last_error().decode(errors="replace"))

@@ -20,9 +20,11 @@ def lib():
     return sa.load()
 
 
-def declared_functions():
+def declared_functions(debug=False):
+    """Functions declared in include/sa.h (the release library's ABI), or in
+    include/sa_debug.h (the SA_DEBUG build's test entry point)."""
     names = set()
-    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+    for h in glob.glob(os.path.join(ROOT, "include", "sa_debug.h" if debug else "sa.h")):
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         names.update(re.findall(r"\b(sa_[a-z0-9_]+)\s*\(", text))
@@ -35,6 +37,24 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
         assert n in sa.SIGNATURES, f"{n} has no binding"
+
+
+def test_headers_are_covered():
+    """Every header in include/ is one of the two checked above and below."""
+    assert sorted(os.path.basename(h) for h in glob.glob(os.path.join(ROOT, "include", "*.h"))) == \
+        ["sa.h", "sa_debug.h"]
+
+
+def test_debug_build_exports_every_declared_symbol():
+    build.build(debug=True)
+    dbg = sa.load_debug()
+    names = declared_functions(debug=True)
+    assert names == ["sa_debug_check_band_items"]
+    for n in names + declared_functions():
+        assert hasattr(dbg, n), n
+        assert n in sa.SIGNATURES or n in sa.DEBUG_SIGNATURES, f"{n} has no binding"
+    rel = sa.load()
+    assert not hasattr(rel, "sa_debug_check_band_items")
 
 
 def test_version(lib):
