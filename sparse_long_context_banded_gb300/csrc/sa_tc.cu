@@ -1343,62 +1343,61 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
           if (ok && pv_item > 0) mma_commit_warp(B.o_final + 8 * u);
         }
       } else {
-      uint32_t pv = 0, jq = 0, g = 0;  // jq: query tiles of earlier items
-      int k_slot = 0, k_par = 0;  // ring position and phase of the next K load
-      bool ok = !p.g_alt;  // (the alternating issuer above has run instead)
-      for (int item = item0; item < n_items && ok; item += stride) {
-        const Work w = make_work<GLOBAL>(P, item);
-        const bool act = u ? w.active[1] : w.active[0];
-        // this tile's load index (a shared tile: one load per item)
-        const uint32_t jt = shared_q ? jq : jq + ((u == 1 && w.active[0]) ? 1u : 0u);
-        jq += shared_q ? 1u : (uint32_t)w.active[0] + (uint32_t)w.active[1];
-        const uint32_t qb = jt % NQ;
-        const uint64_t dq = sw128_desc(s_q0 + qb * C::kQBytes, 16, 1024);
-        if (act) {
-          ok = __all_sync(0xffffffffu, wait_bar(B.q_full + 8 * qb, (jt / NQ) & 1u, abort_flag, p.err));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const int n_tiles = w.nb + w.ng;
-        const int a_u = (u ? w.n_lo[1] : w.n_lo[0]) - w.lo;
-        const int b_u = a_u + (u ? w.n_cnt[1] : w.n_cnt[0]);
-        // last position the tile reads
-        const int last = kGlobalsFirst ? w.ng + b_u - 1 : (w.ng > 0 ? n_tiles - 1 : b_u - 1);
-        int pv_item = 0;
-        for (int i = 0; i <= n_tiles && ok; ++i) {
-          const int v_slot = k_slot == 0 ? NS - 1 : k_slot - 1;
-          const int v_par = k_slot == 0 ? k_par ^ 1 : k_par;
-          const bool do_pv = i > 0, do_s = i < n_tiles;
-          const int ip = i - 1;
-          const bool gp = is_global_pos(w, ip), gc = is_global_pos(w, i);
-          const int ipb = band_index(w, ip), ib = band_index(w, i);
-          const bool pv_reads = do_pv && act && (gp || (ipb >= a_u && ipb < b_u));
-          const bool s_reads = do_s && act && (gc || (ib >= a_u && ib < b_u));
-          // ping-pong handshake (position g of tile 1 follows position g of tile 0)
-          const bool hs = do_s && (u == 1 || g > 0);
-          const uint32_t hs_bar = u == 1 ? B.s_issued : B.s_issued + 8;
-          const uint32_t hs_par = u == 1 ? (g & 1u) : ((g - 1) & 1u);
-          // the slot and handshake conditions are usually met already: poll
-          // them together, block only on P, and wait for what was not met
-          uint32_t pend = 0;
-          if (do_pv && !mbar_test(B.slot_full + 8 * v_slot, v_par)) pend |= 1u;
-          if (do_s && !mbar_test(B.slot_full + 8 * k_slot, k_par)) pend |= 2u;
-          if (hs && !mbar_test(hs_bar, hs_par)) pend |= 4u;
-          pend = __reduce_or_sync(0xffffffffu, pend);
-          if (do_pv) {
-            // a band tile's P arrives in two halves (keys 0-63, then 64-127)
-            if (pv_reads)
-              ok = __all_sync(0xffffffffu, wait_bar(gp ? p_full : B.p_half + 8 * u, pv & 1u, abort_flag, p.err));
-            if (ok && (pend & 1u))
-              ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * v_slot, v_par, abort_flag, p.err));
+        // More global rows than one query tile holds: two query tiles of
+        // different global rows, each over every key tile of the item's chunk,
+        // taken whole.  For position i an issuer does
+        //   PV_u(i-1) [needs P_u(i-1), V_{i-1}], then S_u(i) [needs K_i];
+        // S_u(i) overwrites the TMEM columns P_u(i-1) was read from, and MMAs
+        // of one thread execute in order, so issuing it after PV_u(i-1) is
+        // enough.  P arrives in two halves (keys 0-63, then 64-127), so the
+        // first half of P V starts while the second half of P is computed.  The
+        // two query tiles are kept half a period apart: S_0(g) is issued after
+        // S_1(g-1), and S_1(g) after S_0(g), counting positions g over all
+        // items of the CTA.  An issuer whose query tile is empty releases each
+        // key and value slot by a plain arrive after the tile has landed.
+        uint32_t pv = 0, jq = 0, g = 0;  // jq: query tiles of earlier items
+        int k_slot = 0, k_par = 0;  // ring position and phase of the next K load
+        bool ok = !p.g_alt;  // (the alternating issuer above has run instead)
+        for (int item = item0; item < n_items && ok; item += stride) {
+          const Work w = make_work<GLOBAL>(P, item);
+          const bool act = u ? w.active[1] : w.active[0];
+          const uint32_t jt = jq + ((u == 1 && w.active[0]) ? 1u : 0u);
+          jq += (uint32_t)w.active[0] + (uint32_t)w.active[1];
+          const uint32_t qb = jt % NQ;
+          const uint64_t dq = sw128_desc(s_q0 + qb * C::kQBytes, 16, 1024);
+          if (act) {
+            ok = __all_sync(0xffffffffu, wait_bar(B.q_full + 8 * qb, (jt / NQ) & 1u, abort_flag, p.err));
             if (!ok) break;
-            if (pv_reads) {
-              tc_fence_after();
-              const uint64_t off = (uint64_t)((v_slot * C::kSlotBytes) >> 4);
-              const uint32_t first = pv_item == 0 ? 0u : 1u;
-              // split P (PRECISE): the low parts sit 64 columns after the high
-              // parts and multiply the same value rows
-              if (!gp) {
+            tc_fence_after();
+          }
+          const int n_tiles = w.nb;
+          int pv_item = 0;
+          for (int i = 0; i <= n_tiles && ok; ++i) {
+            const int v_slot = k_slot == 0 ? NS - 1 : k_slot - 1;
+            const int v_par = k_slot == 0 ? k_par ^ 1 : k_par;
+            const bool do_pv = i > 0, do_s = i < n_tiles;
+            // ping-pong hand-off (position g of tile 1 follows position g of tile 0)
+            const bool hs = do_s && (u == 1 || g > 0);
+            const uint32_t hs_bar = u == 1 ? B.s_issued : B.s_issued + 8;
+            const uint32_t hs_par = u == 1 ? (g & 1u) : ((g - 1) & 1u);
+            // the slot and hand-off conditions are usually met already: poll
+            // them together, block only on P, and wait for what was not met
+            uint32_t pend = 0;
+            if (do_pv && !mbar_test(B.slot_full + 8 * v_slot, v_par)) pend |= 1u;
+            if (do_s && !mbar_test(B.slot_full + 8 * k_slot, k_par)) pend |= 2u;
+            if (hs && !mbar_test(hs_bar, hs_par)) pend |= 4u;
+            pend = __reduce_or_sync(0xffffffffu, pend);
+            if (do_pv) {
+              if (act) ok = __all_sync(0xffffffffu, wait_bar(B.p_half + 8 * u, pv & 1u, abort_flag, p.err));
+              if (ok && (pend & 1u))
+                ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * v_slot, v_par, abort_flag, p.err));
+              if (!ok) break;
+              if (act) {
+                tc_fence_after();
+                const uint64_t off = (uint64_t)((v_slot * C::kSlotBytes) >> 4);
+                const uint32_t first = pv_item == 0 ? 0u : 1u;
+                // split P (PRECISE): the low parts sit 64 columns after the high
+                // parts and multiply the same value rows
 #pragma unroll
                 for (int kk = 0; kk < kPvHalf; ++kk)
                   mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_band + off + v_step(kk), kIdescPV,
@@ -1419,61 +1418,43 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
                   for (int kk = kPvHalf; kk < 2 * kPvHalf; ++kk)
                     mma_ts_warp<TF>(d_o, d_s + 64 + kk * 8, dv_band + off + v_step(kk), kIdescPV, 1u);
                 }
+                ++pv;
+                ++pv_item;
+                mma_commit_warp(B.slot_empty + 8 * v_slot);
+                if (i == n_tiles) mma_commit_warp(B.o_final + 8 * u);
               } else {
-#pragma unroll
-                for (int kk = 0; kk < kGKeys / C::kMmaK; ++kk)
-                  mma_ts_warp<TF>(d_o, d_s + kk * 8, dv_glob + off + v_step(kk), kIdescPV,
-                                  kk > 0 ? 1u : first);
-                if constexpr (PRECISE) {
-#pragma unroll
-                  for (int kk = 0; kk < kGKeys / C::kMmaK; ++kk)
-                    mma_ts_warp<TF>(d_o, d_s + 64 + kk * 8, dv_glob + off + v_step(kk), kIdescPV, 1u);
-                }
+                mbar_arrive_warp(B.slot_empty + 8 * v_slot);
               }
-              ++pv;
-              ++pv_item;
-              mma_commit_warp(B.slot_empty + 8 * v_slot);
-              if (ip == last) mma_commit_warp(B.o_final + 8 * u);
-            } else {
-              mbar_arrive_warp(B.slot_empty + 8 * v_slot);
             }
-          }
-          if (do_s) {
-            if (pend & 2u)
-              ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * k_slot, k_par, abort_flag, p.err));
-            if (ok && (pend & 4u)) ok = __all_sync(0xffffffffu, wait_bar(hs_bar, hs_par, abort_flag, p.err));
-            if (!ok) break;
-            if (s_reads) {
-              tc_fence_after();
-              const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
-              // K steps of 32 bytes of a row: four per 128-byte swizzled row
-              // chunk, then on to the next chunk of the tile
-              if (!gc) {
+            if (do_s) {
+              if (pend & 2u)
+                ok = __all_sync(0xffffffffu, wait_bar(B.slot_full + 8 * k_slot, k_par, abort_flag, p.err));
+              if (ok && (pend & 4u)) ok = __all_sync(0xffffffffu, wait_bar(hs_bar, hs_par, abort_flag, p.err));
+              if (!ok) break;
+              if (act) {
+                tc_fence_after();
+                const uint64_t dk = dk_base + (uint64_t)((k_slot * C::kSlotBytes) >> 4);
+                // K steps of 32 bytes of a row: four per 128-byte swizzled row
+                // chunk, then on to the next chunk of the tile
 #pragma unroll
                 for (int kk = 0; kk < D / C::kMmaK; ++kk)
                   mma_ss_warp<TF>(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
                                   dk + (((kk >> 2) * (kKeys * 128) + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
+                mma_commit_warp(s_full);
+                mma_commit_warp(B.slot_empty + 8 * k_slot);
               } else {
-#pragma unroll
-                for (int kk = 0; kk < D / C::kMmaK; ++kk)
-                  mma_ss_warp<TF>(d_s, dq + (((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4),
-                                  dk + (((kk >> 2) * (kGKeys * 128) + (kk & 3) * 32) >> 4), kIdescSg, kk > 0);
+                mbar_arrive_warp(B.slot_empty + 8 * k_slot);
               }
-              mma_commit_warp(s_full);
-              mma_commit_warp(B.slot_empty + 8 * k_slot);
-            } else {
-              mbar_arrive_warp(B.slot_empty + 8 * k_slot);
-            }
-            mbar_arrive_warp(B.s_issued + 8 * u);  // S_u(g) issued (or not needed)
-            ++g;
-            k_slot += 2;  // advance by two loads (K_i, V_i)
-            if (k_slot >= NS) {
-              k_slot -= NS;
-              k_par ^= 1;
+              mbar_arrive_warp(B.s_issued + 8 * u);  // S_u(g) issued (or not needed)
+              ++g;
+              k_slot += 2;  // advance by two loads (K_i, V_i)
+              if (k_slot >= NS) {
+                k_slot -= NS;
+                k_par ^= 1;
+              }
             }
           }
         }
-      }
       }
       // everything this thread issued has completed before TMEM is released
       mma_commit_warp(B.mma_done + 8 * u);
