@@ -264,31 +264,37 @@ __global__ void __launch_bounds__(NT) global_simt_kernel(DevProblem p) {
 // One block per (global row, head); writes that global row of `out` (and lse).
 // Upper bound of the key chunks of the global-row pass (the schedule asks for
 // at most a few hundred CTAs).
-constexpr int kMaxMergeChunks = 1024;  // a multiple of 64 (the smallest block)
+constexpr int kMaxMergeChunks = 1024;  // a multiple of the merge block
+
+constexpr int kMergeThreads = 128;
 
 template <typename T>
-__global__ void merge_kernel(DevProblem p) {
-  // One block per (global row, head), one thread per output column.  Partial x
-  // is row g + 64 (x % part_sub) of set x / part_sub.  The odd set of a chunk
-  // holding a single key tile was never written (g_alt: the chunk's second
-  // query tile had no key tile to take), and a partial that
-  // saw no key has max -inf and sum 0: both get weight 0.  Each partial's
-  // (max, sum) pair is read once, as one 8-byte load; then every thread sums
-  // its column over the partials, sixteen independent loads at a time (a
-  // partial of weight 0 is loaded from a written row and discarded).  The
-  // partials are read in full only after the kernels that write them are done
-  // (launched as a programmatic dependent: the launch itself overlaps them).
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(DevProblem p) {
+  // One block per (global row, head).  Partial x is row g + 64 (x % part_sub)
+  // of set x / part_sub.  The odd set of a chunk holding a single key tile was
+  // never written (g_alt: the chunk's second query tile had no key tile to
+  // take), and a partial that saw no key has max -inf and sum 0: both get
+  // weight 0.  Each partial's (max, sum) pair is read once, as one 8-byte
+  // load.  Then the block sums the partials column by column: thread t takes
+  // four consecutive columns (one 16-byte load per partial) of the partials
+  // x = g, g + G, g + 2G, ... (g = t / (D/4), G = 128 / (D/4) groups), eight
+  // loads in flight at a time, and the G group sums of each column are added
+  // in a fixed order, so the result is the same for every call.  The partials
+  // are read in full only after the kernels that write them are done (launched
+  // as a programmatic dependent: the launch itself overlaps them).
   __shared__ float w_part[kMaxMergeChunks];
   __shared__ int64_t row_part[kMaxMergeChunks];
-  __shared__ float red[8];
+  __shared__ float red[kMergeThreads / 32];
+  __shared__ __align__(16) float colsum[kMergeThreads * 4];  // [group][D]
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int g = blockIdx.x, bh = blockIdx.y, t = threadIdx.x, nt = blockDim.x, nw = nt >> 5;
+  const int g = blockIdx.x, bh = blockIdx.y, t = threadIdx.x;
+  constexpr int nt = kMergeThreads, nw = kMergeThreads / 32;
   const int np = p.part_sets * p.part_sub;
   const int64_t row0 = (int64_t)bh * p.part_sets * p.g_pad + g;  // set 0, first sub-row: written
   float m = -INFINITY;
-  float2 ml[kMaxMergeChunks / 64];  // this thread's partials x = t, t + nt, ...
+  float2 ml[kMaxMergeChunks / nt];  // this thread's partials x = t, t + nt, ...
 #pragma unroll
-  for (int k = 0; k < kMaxMergeChunks / 64; ++k) {
+  for (int k = 0; k < kMaxMergeChunks / nt; ++k) {
     const int x = t + k * nt;
     ml[k] = make_float2(-INFINITY, 0.f);
     if (x < np) {
@@ -309,11 +315,12 @@ __global__ void merge_kernel(DevProblem p) {
   if ((t & 31) == 0) red[t >> 5] = m;
   __syncthreads();
   m = red[0];
+#pragma unroll
   for (int i = 1; i < nw; ++i) m = fmaxf(m, red[i]);
   __syncthreads();
   float l = 0.f;
 #pragma unroll
-  for (int k = 0; k < kMaxMergeChunks / 64; ++k) {
+  for (int k = 0; k < kMaxMergeChunks / nt; ++k) {
     const int x = t + k * nt;
     if (x < np) {
       const float wc = ml[k].x == -INFINITY ? 0.f : exp2f(ml[k].x - m);
@@ -324,31 +331,48 @@ __global__ void merge_kernel(DevProblem p) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   if ((t & 31) == 0) red[t >> 5] = l;
-  __syncthreads();
+  __syncthreads();  // (also: w_part and row_part complete)
   l = red[0];
+#pragma unroll
   for (int i = 1; i < nw; ++i) l += red[i];
-  const float inv = 1.f / l;
-  const int64_t orow = ((int64_t)bh * p.N + p.globals[g]) * p.D;
-  // the same partials in the same order for every column and every call
-  for (int d = t; d < p.D; d += nt) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int x = 0;
-    for (; x + 16 <= np; x += 16) {
-      float v[16];
+  // column sums: thread t, columns 4 (t % q) .. + 3 of the partials x = grp, grp + G, ...
+  const int q = p.D / 4, G = nt / q, grp = t / q, c4 = t - grp * q;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int x = grp;
+  for (; x + 7 * G < np; x += 8 * G) {
+    float4 v[8];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = p.part_o[row_part[x + k] * p.D + d];
+    for (int k = 0; k < 8; ++k)
+      v[k] = reinterpret_cast<const float4 *>(p.part_o + row_part[x + k * G] * p.D)[c4];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float wk = w_part[x + k];
-        acc[k & 3] += wk != 0.f ? v[k] * wk : 0.f;
+    for (int k = 0; k < 8; ++k) {
+      const float wk = w_part[x + k * G];
+      if (wk != 0.f) {
+        acc.x += v[k].x * wk;
+        acc.y += v[k].y * wk;
+        acc.z += v[k].z * wk;
+        acc.w += v[k].w * wk;
       }
     }
-    for (; x < np; ++x) {
-      const float wk = w_part[x];
-      const float vk = p.part_o[row_part[x] * p.D + d];
-      acc[0] += wk != 0.f ? vk * wk : 0.f;
+  }
+  for (; x < np; x += G) {
+    const float wk = w_part[x];
+    const float4 vk = reinterpret_cast<const float4 *>(p.part_o + row_part[x] * p.D)[c4];
+    if (wk != 0.f) {
+      acc.x += vk.x * wk;
+      acc.y += vk.y * wk;
+      acc.z += vk.z * wk;
+      acc.w += vk.w * wk;
     }
-    st<T>(p.out, orow + d, ((acc[0] + acc[1]) + (acc[2] + acc[3])) * inv);
+  }
+  reinterpret_cast<float4 *>(colsum)[grp * q + c4] = acc;
+  __syncthreads();
+  const float inv = 1.f / l;
+  const int64_t orow = ((int64_t)bh * p.N + p.globals[g]) * p.D;
+  for (int d = t; d < p.D; d += nt) {
+    float sum = 0.f;
+    for (int k = 0; k < G; ++k) sum += colsum[k * p.D + d];
+    st<T>(p.out, orow + d, sum * inv);
   }
   if (p.lse && t == 0)
     p.lse[(int64_t)bh * p.N + p.globals[g]] = (m + log2f(l)) * 0.6931471805599453f;
@@ -428,12 +452,12 @@ cudaError_t launch_global_simt(const DevProblem &p, sa_dtype dt, cudaStream_t s)
 
 cudaError_t launch_merge(const DevProblem &p, int BH, sa_dtype dt, cudaStream_t s) {
   if (p.part_sets * p.part_sub > kMaxMergeChunks) return cudaErrorInvalidValue;
-  // one thread per output column (64 or 128); a programmatic dependent launch,
-  // so that the launch overlaps the kernels before it (the kernel waits for
-  // them with griddepcontrol.wait before it reads anything)
+  // 128 threads per (global row, head); a programmatic dependent launch, so
+  // that the launch overlaps the kernels before it (the kernel waits for them
+  // with griddepcontrol.wait before it reads anything)
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p.n_g, BH);
-  cfg.blockDim = dim3(p.D);
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr{};
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -75,6 +75,9 @@ SMALL_CASES = [
     (1, 1, 2050, 64, 600, [4], list(range(0, 2050, 97)), "bf16"),
     (1, 2, 1500, 64, 255, [1, 2], [3, 1499], "bf16"),    # odd window: half width 127
     (1, 2, 2000, 128, 511, [1, 3], [7, 100, 1999], "bf16"),
+    # bands narrower than a 64-key sub-tile: whole sub-tiles masked for some rows
+    (1, 2, 1111, 128, 100, [1, 3], [17], "bf16"),
+    (1, 1, 4500, 64, 62, [2], [], "bf16"),
 ]
 
 
