@@ -353,3 +353,47 @@ def test_profile_counts_launches():
     sa.forward(q32, q32, q32, 64, None, [3, 100])
     prof = sa.profile_end()
     assert [prof[s]["launches"] for s in sa.STAGES] == [1, 1, 1, 1]
+
+
+def test_concurrent_threads_and_streams():
+    """Two host threads, each on a stream of its own, call the library at the
+    same time with different problem shapes (different schedules, scratch from
+    the same pool); every result equals the same call made alone."""
+    import threading
+
+    import torch
+    problems = [
+        (make(1, 2, 3000, 64, "bf16", seed=11), 256, [1, 2], [0, 17, 2999]),
+        (make(1, 2, 2304, 128, "bf16", seed=12), 1024, [1, 1], list(range(64))),
+    ]
+    dev = [[to_device(a, torch) for a in qkv] for qkv, _, _, _ in problems]
+    alone = []
+    for (qkv, window, dil, G), (tq, tk, tv) in zip(problems, dev):
+        alone.append(sa.forward(tq, tk, tv, window, dil, G))
+    torch.cuda.synchronize()
+    sa.sync_status()
+    results = [[], []]
+    errors = []
+
+    def worker(i):
+        try:
+            (qkv, window, dil, G), (tq, tk, tv) = problems[i], dev[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    results[i].append(sa.forward(tq, tk, tv, window, dil, G))
+            s.synchronize()
+            sa.sync_status(s)
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(2):
+        assert len(results[i]) == 20
+        for r in results[i]:
+            assert torch.equal(r, alone[i])
