@@ -36,6 +36,14 @@
  *  - Validation happens before anything is launched; on any non-OK status
  *    nothing was enqueued and sa_last_error() describes the problem.
  *  - Thread safety: calls may come from several host threads and streams.
+ *  - Stream capture: a call may be captured into a CUDA graph once a call of
+ *    the same problem (B, H, N, D, window, dilation, global set, pattern) has
+ *    run on the device outside capture -- that call builds and uploads the
+ *    schedule.  A first call under capture returns SA_ERR_INVALID_ARG with
+ *    nothing captured.  The schedule of a captured call is kept for the life
+ *    of the process (the graph may replay at any time); its scratch is taken
+ *    and returned by the graph's own stream-ordered allocation nodes.
+ *    Profiling (sa_profile_begin) records no events for captured calls.
  */
 #ifndef SA_H_
 #define SA_H_

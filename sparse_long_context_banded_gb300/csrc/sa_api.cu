@@ -280,9 +280,11 @@ struct StageTimer {
   int stage;
   cudaStream_t stream;
   cudaEvent_t start = nullptr;
-  StageTimer(int s, cudaStream_t st) : stage(s), stream(st) {
+  // (no events for a call under stream capture: the graph would record them
+  // at each replay, after the profile has been read)
+  StageTimer(int s, cudaStream_t st, bool capturing) : stage(s), stream(st) {
     std::lock_guard<std::mutex> lock(g_prof.mutex);
-    if (g_prof.on) {
+    if (g_prof.on && !capturing) {
       start = g_prof.get();
       cudaEventRecord(start, stream);
     }
@@ -514,7 +516,7 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   auto step = [&](int stage, const char *range, auto &&launch, const char *what, int launches = 1) {
     if (result != SA_OK) return;
     nvtxRangePushA(range);
-    StageTimer timer(stage, stream);
+    StageTimer timer(stage, stream, capturing);
     cudaError_t le = launch();
     timer.done(launches);
     nvtxRangePop();
@@ -657,7 +659,9 @@ extern "C" sa_status sa_forward_gather(const void *q, const void *k, const void 
   gp.D = D;
   gp.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  StageTimer timer(1, s);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+  StageTimer timer(1, s, cs != cudaStreamCaptureStatusNone);
   cudaError_t e = launch_gather_attention(gp, dtype, s);
   timer.done();
   if (e != cudaSuccess) return cuda_fail(e, "list-gather attention launch");

@@ -397,3 +397,53 @@ def test_concurrent_threads_and_streams():
         assert len(results[i]) == 20
         for r in results[i]:
             assert torch.equal(r, alone[i])
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
+def test_cuda_graph_capture_and_replay():
+    """A call captured into a CUDA graph (after one call of the same shape
+    outside capture, which builds the schedule) replays with new input values
+    and gives exactly what an eager call gives; a first call under capture is
+    refused before anything is enqueued."""
+    import torch
+    B, H, N, D, window, dil, G = 1, 2, 2304, 128, 1024, [1, 1], list(range(64))
+    q0, k0, v0 = make(B, H, N, D, "bf16", seed=21)
+    tq, tk, tv = (to_device(a, torch) for a in (q0, k0, v0))
+    out = torch.empty_like(tq)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    sa.forward(tq, tk, tv, window, dil, G, out=out, lse=lse)  # builds the schedule
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        sa.forward(tq, tk, tv, window, dil, G, out=out, lse=lse, stream=s)  # warm on this stream
+        s.synchronize()
+        with torch.cuda.graph(graph, stream=s):
+            sa.forward(tq, tk, tv, window, dil, G, out=out, lse=lse, stream=s)
+    torch.cuda.synchronize()
+    for seed in (22, 23):
+        q1, k1, v1 = make(B, H, N, D, "bf16", seed=seed)
+        for dst, src in zip((tq, tk, tv), (q1, k1, v1)):
+            dst.copy_(to_device(src, torch))
+        graph.replay()
+        torch.cuda.synchronize()
+        sa.sync_status()
+        got, got_lse = out.clone(), lse.clone()
+        ref_lse = torch.empty_like(lse)
+        ref = sa.forward(tq, tk, tv, window, dil, G, lse=ref_lse)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+        assert torch.equal(got_lse, ref_lse)
+    # a shape never run outside capture: refused, nothing captured
+    small = torch.zeros((1, 2, 1000, D), dtype=torch.bfloat16, device="cuda")
+    small_out = torch.empty_like(small)
+    g2 = torch.cuda.CUDAGraph()
+    status = None
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g2, stream=s):
+            try:
+                sa.forward(small, small, small, 333, dil, [5], out=small_out, stream=s)
+            except sa.SaError as e:
+                status = e.status
+    assert status == sa.SA_ERR_INVALID_ARG
