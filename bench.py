@@ -63,6 +63,9 @@ def parse():
                     help="fp32 workloads: tf32 products on the tensor cores (SA_TF32)")
     ap.add_argument("--heads", type=int, default=0,
                     help="run the workload with this many heads (profiling a smaller case)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one call captured in a CUDA graph (after the eager "
+                         "warm-up); the per-stage pass and e2e stay eager")
     return ap.parse_args()
 
 
@@ -306,14 +309,34 @@ def run_ours(args):
 
     tf32 = bool(args.tf32) and w.dtype == "fp32"
 
-    def step():
+    def eager_step():
         sa.forward(q, k, v, w.window, w.dilation, w.globals_, scale=w.scale, out=out, stream=stream,
                    tf32=tf32)
 
+    step = eager_step
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     sa.sync_status(stream)
+    if args.graph:
+        # one call captured on a side stream (the first eager calls built the
+        # schedule); the timed steps replay it on the launching stream
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                sa.forward(q, k, v, w.window, w.dilation, w.globals_, scale=w.scale, out=out,
+                           stream=side, tf32=tf32)
+        torch.cuda.synchronize()
+
+        def step():
+            graph.replay()
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        sa.sync_status(stream)
 
     # inputs smaller than L2 (129 MB): write a 512 MB buffer between steps, outside
     # the per-step events, so that no step finds its inputs in L2
@@ -358,7 +381,7 @@ def run_ours(args):
     for _ in range(prof_steps):
         if flush is not None:
             flush.zero_()
-        step()
+        eager_step()
     torch.cuda.synchronize()
     prof = sa.profile_end()
     launches_per_step = sum(p["launches"] for p in prof.values()) / prof_steps
@@ -450,6 +473,8 @@ def run_ours(args):
                        "window": w.window, "n_globals": len(w.globals_),
                        "in_mask_pairs_per_step": pairs * world,
                        "in_mask_gflop_per_step": flops_step * world / 1e9,
+                       "launch": "CUDA graph replay of one captured call" if args.graph
+                       else "eager sa.forward calls",
                        "l2": (f"inputs ({in_bytes / 1e9:.2f} GB) larger than L2; no flush"
                               if flush is None else
                               f"inputs ({in_bytes / 1e6:.0f} MB) smaller than L2: a 512 MB "
