@@ -8,7 +8,9 @@ global-row split-K pass, merge (the global rows are contiguous, so they are read
 in place; a scattered set adds a gather).  The metric is useful
 (in-mask) attention FLOP/s: 4*D per scored (query, key) pair, pairs counted
 exactly by sa_count_pairs.  Inputs (1.6 GB) are larger than the 129 MB L2, so
-no flush is needed between steps.
+no flush is needed between steps.  The ``e2e`` key times the same work from
+host memory: one sa_forward_host call per step on pinned q, k, v (copies in,
+attention, copy of the output back, inside the call and the timed region).
 
 Prints ONE JSON line on rank 0.  Under torchrun each rank runs its own
 independent batch (weak scaling) and the time is the max over ranks.
@@ -395,64 +397,36 @@ def run_ours(args):
     kern_tflops = kern_flops / (kern_ms * 1e-3) / 1e12
     traffic, traffic_src = measured_traffic(args.workload) if not args.heads else (None, "")
 
-    # end to end through the public call: every step copies its inputs in from
-    # pinned host memory and its result back out.  Steps are pipelined over two
-    # device buffer sets and three streams (inputs of step i+1 copied in, and
-    # the result of step i-1 copied out, while step i computes), as a serving
-    # loop would run them.
+    # end to end through the C ABI with host buffers: every step is one
+    # sa_forward_host call on pinned q, k, v, which copies them in, runs the
+    # attention and copies the output back, overlapping the copies of one
+    # group of heads with the computation of another; the call returns when
+    # the output is in host memory, so the host clock times it
     e2e = None
     if not args.no_e2e:
         pq, pk_, pv = (t.pin_memory() for t in (hq, hk, hv))
-        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-        bufs = [(q, k, v, out), tuple(torch.empty_like(x) for x in (q, k, v, out))]
-        s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in", "cmp", "out")}
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
-        def e2e_steps_run(n):
-            for i in range(n):
-                b = i % 2
-                dq, dk, dv, dout = bufs[b]
-                if i >= 2:
-                    s_in.wait_event(ev["cmp"][b])   # step i-2 has read this input set
-                with torch.cuda.stream(s_in):
-                    dq.copy_(pq, non_blocking=True)
-                    dk.copy_(pk_, non_blocking=True)
-                    dv.copy_(pv, non_blocking=True)
-                ev["in"][b].record(s_in)
-                s_cmp.wait_event(ev["in"][b])
-                if i >= 2:
-                    s_cmp.wait_event(ev["out"][b])  # step i-2's result has been copied out
-                sa.forward(dq, dk, dv, w.window, w.dilation, w.globals_, scale=w.scale, out=dout,
-                           stream=s_cmp, tf32=tf32)
-                ev["cmp"][b].record(s_cmp)
-                s_out.wait_event(ev["cmp"][b])
-                with torch.cuda.stream(s_out):
-                    hout[b].copy_(dout, non_blocking=True)
-                ev["out"][b].record(s_out)
+        def host_step():
+            sa.forward_host(pq, pk_, pv, w.window, w.dilation, w.globals_, scale=w.scale,
+                            out=hout, tf32=tf32, device=dev)
 
-        e2e_steps_run(2)
-        torch.cuda.synchronize()
+        for _ in range(2):
+            host_step()
         e2e_steps = max(4, min(args.steps, 12))
         barrier(world)
         torch.cuda.synchronize()
-        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        x0.record(s_in)
-        s_cmp.wait_event(x0)
-        s_out.wait_event(x0)
-        e2e_steps_run(e2e_steps)
-        s_out.wait_stream(s_in)
-        s_out.wait_stream(s_cmp)
-        x1.record(s_out)
-        torch.cuda.synchronize()
-        sa.sync_status(s_cmp)
-        ms_e2e = max_over_ranks(x0.elapsed_time(x1), world, dev)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            host_step()
+        ms_e2e = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
         h2d = 3 * q.numel() * q.element_size()
         d2h = out.numel() * out.element_size()
         e2e = {"value": world * flops_step * e2e_steps / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ms_e2e / e2e_steps, "steps": e2e_steps,
-               "pipelined": "step i+1's inputs copied in and step i-1's result copied out "
-                            "while step i computes (two buffer sets, three streams)"}
+               "call": "sa_forward_host on pinned host tensors (copies in, attention, copy "
+                       "out; groups of heads pipelined inside the call)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

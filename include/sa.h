@@ -27,6 +27,7 @@
  * Conventions for every entry point:
  *  - Tensors are device pointers, contiguous [B, H, N, D] with D fastest,
  *    16-byte aligned; the caller owns them.  q, k, v, out share one dtype.
+ *    (sa_forward_host alone takes host buffers, and is synchronous.)
  *  - Host arrays (dilation, global_idx) are read during the call only; the
  *    caller may free them on return.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
@@ -177,6 +178,41 @@ sa_status sa_forward_global_proj(const void *q, const void *k, const void *v,
                                  int N, int D, int window, const int32_t *dilation,
                                  const int32_t *global_idx, int n_global, float scale,
                                  sa_dtype dtype, sa_stream_t stream);
+
+/*
+ * sa_forward_host -- sa_forward_lse on host buffers: the inputs are copied to
+ * the current device, the attention runs there, and out (and lse) are copied
+ * back; the call returns when they are written (synchronous).
+ *
+ * Every (b, h) slice is a problem of its own (its band, its global rows and
+ * its output involve that slice only), so the call cuts the slices into
+ * groups of consecutive heads and pipelines them over two sets of device
+ * buffers on three streams of its own: group g+1's inputs are copied in while
+ * group g is computed and group g-1's output is copied out.
+ *
+ *  q, k, v   host, [B,H,N,D] in `dtype`, contiguous; read only.  Page-locked
+ *            memory (cudaHostAlloc, cudaHostRegister) lets the copies run
+ *            asynchronously and overlap the computation; pageable memory
+ *            gives the same result with the copies serialised on the host.
+ *  out       host, [B,H,N,D] in `dtype`; fully written.
+ *  lse       host, [B,H,N] float32, or NULL.
+ *  heads_per_group  slices per group: 0 lets the library choose (about eight
+ *            groups of at least 32 MiB of inputs each); a value below H splits
+ *            each batch element's heads into groups of that many; H or more
+ *            takes floor(heads_per_group / H) whole batch elements per group.
+ *  Other arguments: as sa_forward (no alignment rule for the host buffers).
+ *
+ * Device memory: two buffer sets of one group's q, k, v, out (and lse) from
+ * the library's stream-ordered pool, plus each group's sa_forward scratch;
+ * SA_ERR_NO_MEMORY if they cannot be had.  Every argument is checked before
+ * any copy.  On any status, everything the call enqueued has finished when it
+ * returns.  Like sa_sync_status, it reports (and clears) the device error
+ * word at the end: SA_ERR_TIMEOUT if a kernel gave up on a stalled wait.
+ */
+sa_status sa_forward_host(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int B, int H, int N, int D, int window, const int32_t *dilation,
+                          const int32_t *global_idx, int n_global, float scale, sa_dtype dtype,
+                          int heads_per_group);
 
 /*
  * sa_count_pairs -- exact number of (i, j) pairs in the mask, |S_i| summed

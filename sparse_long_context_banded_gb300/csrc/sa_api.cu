@@ -17,6 +17,7 @@
 // empty.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -336,29 +337,16 @@ bool split_p(const Problem &p) {
 
 // ---------------------------------------------------------------------------
 
-sa_status forward_impl(const void *q, const void *k, const void *v, void *out, float *lse,
-                       int B, int H, int N, int D, int window, const int32_t *dilation,
-                       const int32_t *global_idx, int n_global, float scale, sa_dtype dtype,
-                       cudaStream_t stream, int chunk = 0, int memory = 0,
-                       const void *q_glob = nullptr, const void *k_glob = nullptr,
-                       const void *v_glob = nullptr) {
-  if (!q || !k || !v || !out) return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be non-null");
-  if (!q_glob) q_glob = q;
-  if (!k_glob) k_glob = k;
-  if (!v_glob) v_glob = v;
+// The problem of one call, checked before anything is enqueued: every
+// argument but the device pointers.
+sa_status build_problem(int B, int H, int N, int D, int window, const int32_t *dilation,
+                        const int32_t *global_idx, int n_global, float scale, sa_dtype dtype,
+                        int chunk, int memory, Problem *out) {
   if (n_global < 0) return fail(SA_ERR_INVALID_ARG, "n_global must be >= 0");
   if (n_global > 0 && !global_idx)
     return fail(SA_ERR_INVALID_ARG, "global_idx is null but n_global = %d", n_global);
   if (H < 1) return fail(SA_ERR_INVALID_ARG, "H must be >= 1 (got %d)", H);
-  const void *ptrs[7] = {q, k, v, out, q_glob, k_glob, v_glob};
-  for (int i = 0; i < 7; ++i)
-    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0)
-      return fail(SA_ERR_INVALID_ARG, "q, k, v, out (and the global projections) must be "
-                  "16-byte aligned");
-  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0)
-    return fail(SA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
-
-  Problem p;
+  Problem &p = *out;
   p.B = B;
   p.H = H;
   p.N = N;
@@ -383,6 +371,32 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   if ((int)p.globals.size() > SA_MAX_GLOBALS)
     return fail(SA_ERR_UNSUPPORTED, "%d distinct globals (at most %d)", (int)p.globals.size(),
                 SA_MAX_GLOBALS);
+  if (dtype == SA_TF32 && !tc_supports(dtype, D))
+    return fail(SA_ERR_UNSUPPORTED, "SA_TF32 supports D = 64 (got %d)", D);
+  return SA_OK;
+}
+
+sa_status forward_impl(const void *q, const void *k, const void *v, void *out, float *lse,
+                       int B, int H, int N, int D, int window, const int32_t *dilation,
+                       const int32_t *global_idx, int n_global, float scale, sa_dtype dtype,
+                       cudaStream_t stream, int chunk = 0, int memory = 0,
+                       const void *q_glob = nullptr, const void *k_glob = nullptr,
+                       const void *v_glob = nullptr) {
+  if (!q || !k || !v || !out) return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be non-null");
+  if (!q_glob) q_glob = q;
+  if (!k_glob) k_glob = k;
+  if (!v_glob) v_glob = v;
+  const void *ptrs[7] = {q, k, v, out, q_glob, k_glob, v_glob};
+  for (int i = 0; i < 7; ++i)
+    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0)
+      return fail(SA_ERR_INVALID_ARG, "q, k, v, out (and the global projections) must be "
+                  "16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0)
+    return fail(SA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  Problem p;
+  sa_status vst = build_problem(B, H, N, D, window, dilation, global_idx, n_global, scale, dtype,
+                                chunk, memory, &p);
+  if (vst != SA_OK) return vst;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -394,8 +408,6 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
 
   // bf16 -> tensor cores (kind::f16); tf32 (fp32 in memory, D = 64) -> tensor
   // cores (kind::tf32, no cast of the inputs); fp32 -> CUDA cores, fp32 throughout
-  if (dtype == SA_TF32 && !tc_supports(dtype, D))
-    return fail(SA_ERR_UNSUPPORTED, "SA_TF32 supports D = 64 (got %d)", D);
   const bool tc = tc_supports(dtype, D);
   const bool precise = tc && dtype == SA_BF16 && split_p(p);
 
@@ -625,6 +637,165 @@ extern "C" sa_status sa_forward_global_proj(const void *q, const void *k, const 
   return forward_impl(q, k, v, out, lse, B, H, N, D, window, dilation, global_idx, n_global,
                       scale, dtype, reinterpret_cast<cudaStream_t>(stream), 0, 0, q_global,
                       k_global, v_global);
+}
+
+// ---------------------------------------------------------------------------
+// Host buffers.  Each (b, h) slice is a problem of its own (its mask, its
+// global rows and its output involve that slice only), so the call cuts the
+// slices into groups of consecutive heads and runs a three-stage pipeline
+// over two sets of device buffers: group g+1's inputs are copied in while
+// group g is computed and group g-1's output is copied out.
+
+namespace sa {
+namespace {
+
+constexpr int kHostGroups = 8;                       // groups wanted per call
+constexpr int64_t kHostGroupMinBytes = 32ll << 20;   // inputs of one group, at least
+
+// Batches b0 .. b0+nb-1, heads h0 .. h0+nh-1 of each (nb > 1 only with all heads).
+struct HostGroup {
+  int b0, nb, h0, nh;
+};
+
+std::vector<HostGroup> host_groups(int B, int H, int64_t head_input_bytes, int heads_per_group) {
+  const int64_t units = (int64_t)B * H;
+  int64_t g = heads_per_group;
+  if (g <= 0) {
+    const int64_t min_heads = (kHostGroupMinBytes + head_input_bytes - 1) / head_input_bytes;
+    g = std::max<int64_t>({(units + kHostGroups - 1) / kHostGroups, min_heads, 1});
+  }
+  std::vector<HostGroup> groups;
+  if (g < H) {
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; h += (int)g) groups.push_back({b, 1, h, (int)std::min<int64_t>(g, H - h)});
+  } else {
+    const int nb = (int)std::min<int64_t>(B, g / H);
+    for (int b = 0; b < B; b += nb) groups.push_back({b, std::min(nb, B - b), 0, H});
+  }
+  return groups;
+}
+
+}  // namespace
+}  // namespace sa
+
+extern "C" sa_status sa_forward_host(const void *q, const void *k, const void *v, void *out,
+                                     float *lse, int B, int H, int N, int D, int window,
+                                     const int32_t *dilation, const int32_t *global_idx,
+                                     int n_global, float scale, sa_dtype dtype,
+                                     int heads_per_group) {
+  if (!q || !k || !v || !out) return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be non-null");
+  if (heads_per_group < 0)
+    return fail(SA_ERR_INVALID_ARG, "heads_per_group must be >= 0 (got %d)", heads_per_group);
+  {
+    Problem p;  // every argument checked before any copy
+    sa_status st = build_problem(B, H, N, D, window, dilation, global_idx, n_global, scale, dtype,
+                                 0, 0, &p);
+    if (st != SA_OK) return st;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState *ds = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    sa_status st = device_state(dev, &ds);
+    if (st != SA_OK) return st;
+  }
+  const size_t es = dtype == SA_BF16 ? 2 : 4;
+  const size_t head_elems = (size_t)N * D;
+  const std::vector<HostGroup> groups =
+      host_groups(B, H, (int64_t)(3 * head_elems * es), heads_per_group);
+  size_t max_heads = 0;
+  for (const HostGroup &g : groups) max_heads = std::max(max_heads, (size_t)g.nb * g.nh);
+  auto round256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t r = round256(max_heads * head_elems * es);  // one tensor of one set
+  const size_t set_bytes = 4 * r + (lse ? round256(max_heads * N * sizeof(float)) : 0);
+
+  // stages: 0 copies in, 1 computes, 2 copies out; per buffer set, the event
+  // each stage records after its work on that set
+  cudaStream_t st[3] = {nullptr, nullptr, nullptr};
+  cudaEvent_t ev[3][2] = {};
+  char *set[2] = {nullptr, nullptr};
+  sa_status result = SA_OK;
+  auto check = [&result](cudaError_t ce, const char *what) {
+    if (ce != cudaSuccess && result == SA_OK) result = cuda_fail(ce, what);
+    return result == SA_OK;
+  };
+  for (int i = 0; i < 3 && result == SA_OK; ++i)
+    check(cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking), "cudaStreamCreate");
+  for (int i = 0; i < 3 && result == SA_OK; ++i)
+    for (int b = 0; b < 2 && result == SA_OK; ++b)
+      check(cudaEventCreateWithFlags(&ev[i][b], cudaEventDisableTiming), "cudaEventCreate");
+  // both sets are allocated on the copy-in stream; every later use waits for
+  // an event recorded there after the allocation
+  for (int b = 0; b < 2 && result == SA_OK && b < (int)groups.size(); ++b) {
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&set[b]), set_bytes, ds->pool, st[0]);
+    if (e != cudaSuccess)
+      result = fail(SA_ERR_NO_MEMORY, "host-call buffers of %zu bytes: %s", set_bytes,
+                    cudaGetErrorString(e));
+  }
+  for (size_t gi = 0; gi < groups.size() && result == SA_OK; ++gi) {
+    const HostGroup &g = groups[gi];
+    const int b = (int)(gi & 1);
+    const size_t u0 = (size_t)g.b0 * H + g.h0, nu = (size_t)g.nb * g.nh;
+    const size_t off = u0 * head_elems * es, bytes = nu * head_elems * es;
+    char *dq = set[b], *dk = dq + r, *dv = dk + r, *dout = dv + r;
+    float *dlse = lse ? reinterpret_cast<float *>(dout + r) : nullptr;
+    // group gi-2 used this set: its inputs must have been read before they are
+    // overwritten, its output copied out before it is overwritten
+    if (gi >= 2 && !check(cudaStreamWaitEvent(st[0], ev[1][b], 0), "cudaStreamWaitEvent")) break;
+    if (!check(cudaMemcpyAsync(dq, static_cast<const char *>(q) + off, bytes,
+                               cudaMemcpyHostToDevice, st[0]), "copy of q to the device") ||
+        !check(cudaMemcpyAsync(dk, static_cast<const char *>(k) + off, bytes,
+                               cudaMemcpyHostToDevice, st[0]), "copy of k to the device") ||
+        !check(cudaMemcpyAsync(dv, static_cast<const char *>(v) + off, bytes,
+                               cudaMemcpyHostToDevice, st[0]), "copy of v to the device") ||
+        !check(cudaEventRecord(ev[0][b], st[0]), "cudaEventRecord") ||
+        !check(cudaStreamWaitEvent(st[1], ev[0][b], 0), "cudaStreamWaitEvent") ||
+        (gi >= 2 && !check(cudaStreamWaitEvent(st[1], ev[2][b], 0), "cudaStreamWaitEvent")))
+      break;
+    sa_status fs = forward_impl(dq, dk, dv, dout, dlse, g.nb, g.nh, N, D, window,
+                                dilation ? dilation + g.h0 : nullptr, global_idx, n_global, scale,
+                                dtype, st[1]);
+    if (fs != SA_OK) {
+      result = fs;
+      break;
+    }
+    if (!check(cudaEventRecord(ev[1][b], st[1]), "cudaEventRecord") ||
+        !check(cudaStreamWaitEvent(st[2], ev[1][b], 0), "cudaStreamWaitEvent") ||
+        !check(cudaMemcpyAsync(static_cast<char *>(out) + off, dout, bytes,
+                               cudaMemcpyDeviceToHost, st[2]), "copy of out to the host") ||
+        (lse && !check(cudaMemcpyAsync(lse + u0 * N, dlse, nu * N * sizeof(float),
+                                       cudaMemcpyDeviceToHost, st[2]), "copy of lse to the host")) ||
+        !check(cudaEventRecord(ev[2][b], st[2]), "cudaEventRecord"))
+      break;
+  }
+  // whatever was enqueued finishes before the host buffers are handed back
+  // (a failure here is reported only when nothing failed before)
+  for (int i = 0; i < 3; ++i)
+    if (st[i]) check(cudaStreamSynchronize(st[i]), "stream synchronize");
+  for (int b = 0; b < 2; ++b)
+    if (set[b]) {
+      check(cudaFreeAsync(set[b], st[2]), "cudaFreeAsync(host-call buffers)");
+      check(cudaStreamSynchronize(st[2]), "stream synchronize");
+    }
+  for (int i = 0; i < 3; ++i)
+    for (int b = 0; b < 2; ++b)
+      if (ev[i][b]) cudaEventDestroy(ev[i][b]);
+  for (int i = 0; i < 3; ++i)
+    if (st[i]) cudaStreamDestroy(st[i]);
+  if (result != SA_OK) return result;
+  // the device error word, as sa_sync_status reports it
+  int word = 0;
+  e = cudaMemcpy(&word, ds->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (word != 0) {
+    cudaMemset(ds->err, 0, sizeof(int));
+    if (word & kErrWaitTimeout)
+      return fail(SA_ERR_TIMEOUT, "a kernel gave up on a stalled wait (error word 0x%x)", word);
+    return fail(SA_ERR_CUDA, "a kernel failed a device-side check (error word 0x%x)", word);
+  }
+  return SA_OK;
 }
 
 extern "C" sa_status sa_forward_gather(const void *q, const void *k, const void *v,

@@ -52,6 +52,8 @@ SIGNATURES = {
                                _VP]),
     "sa_forward_global_proj": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I,
                                     _I32P, _I32P, _I, _F, _I, _VP]),
+    "sa_forward_host": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I32P, _I32P, _I, _F,
+                             _I, _I]),
     "sa_set_pv_mode": (_I, [_I]),
     "sa_get_pv_mode": (_I, []),
     "sa_uses_split_p": (_I, [_I, _I, _I, _I32P, _I, _I32P, _I, _I, _I, _F]),
@@ -190,6 +192,51 @@ def forward(q, k, v, window: int, dilation: Sequence[int] | None = None,
             st = load().sa_forward_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                        lse.data_ptr(), B, H, N, D, int(window), _ptr(dil),
                                        _ptr(g), int(g.size), sc, dt, h_stream)
+    _check(st)
+    return out
+
+
+def forward_host(q, k, v, window: int, dilation: Sequence[int] | None = None,
+                 globals_: Sequence[int] = (), scale: Optional[float] = None, out=None,
+                 lse=None, tf32: bool = False, heads_per_group: int = 0, device=None):
+    """``forward`` on host (CPU) torch tensors: sa_forward_host copies them to
+    ``device`` (default: the current CUDA device), runs the attention and
+    copies ``out`` (and ``lse``, a float32 CPU tensor [B, H, N]) back, with the
+    copies of one group of heads overlapping the computation of another.
+    Pinned tensors (``.pin_memory()``) let the copies overlap.  Synchronous;
+    returns ``out``.
+    """
+    import torch
+
+    if q.dtype == torch.bfloat16:
+        dt = SA_BF16
+    elif q.dtype == torch.float32:
+        dt = SA_TF32 if tf32 else SA_FP32
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype} (bfloat16 or float32)")
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or t.shape != q.shape:
+            raise ValueError("q, k, v must be contiguous CPU tensors of one shape and dtype")
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, D]")
+    B, H, N, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if out.is_cuda or not out.is_contiguous() or out.dtype != q.dtype or out.shape != q.shape:
+        raise ValueError("out must be a contiguous CPU tensor like q")
+    if lse is not None and (lse.is_cuda or not lse.is_contiguous() or lse.dtype != torch.float32
+                            or tuple(lse.shape) != (B, H, N)):
+        raise ValueError("lse must be a contiguous float32 CPU tensor [B, H, N]")
+    dil = None if dilation is None else _i32(dilation)
+    if dil is not None and dil.size != H:
+        raise ValueError("dilation needs one entry per head")
+    g = _i32(globals_)
+    sc = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = load().sa_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    None if lse is None else lse.data_ptr(), B, H, N, D,
+                                    int(window), _ptr(dil), _ptr(g), int(g.size), sc, dt,
+                                    int(heads_per_group))
     _check(st)
     return out
 

@@ -143,6 +143,40 @@ def test_forward_rejects_bad_arguments(lib, kwargs, status):
     assert lib.sa_last_error().decode()
 
 
+def _fwd_host(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, H=2, N=64, D=64, window=8,
+              dilation=None, g=None, ng=0, scale=0.125, dtype=sa.SA_BF16, heads_per_group=0):
+    dil = None if dilation is None else np.asarray(dilation, dtype=np.int32)
+    gg = None if g is None else np.asarray(g, dtype=np.int32)
+    return lib.sa_forward_host(q, k, v, out, None, B, H, N, D, window,
+                               None if dil is None else dil.ctypes.data_as(ctypes.c_void_p),
+                               None if gg is None else gg.ctypes.data_as(ctypes.c_void_p),
+                               ng, scale, dtype, heads_per_group)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(q=None), sa.SA_ERR_INVALID_ARG),
+    (dict(out=None), sa.SA_ERR_INVALID_ARG),
+    (dict(N=0), sa.SA_ERR_INVALID_ARG),
+    (dict(B=0), sa.SA_ERR_INVALID_ARG),
+    (dict(H=0), sa.SA_ERR_INVALID_ARG),
+    (dict(window=-1), sa.SA_ERR_INVALID_ARG),
+    (dict(dilation=[1, 0]), sa.SA_ERR_INVALID_ARG),
+    (dict(g=[64], ng=1), sa.SA_ERR_INVALID_ARG),
+    (dict(g=None, ng=3), sa.SA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), sa.SA_ERR_INVALID_ARG),
+    (dict(dtype=7), sa.SA_ERR_INVALID_ARG),
+    (dict(heads_per_group=-1), sa.SA_ERR_INVALID_ARG),
+    (dict(D=96), sa.SA_ERR_UNSUPPORTED),
+    (dict(D=128, dtype=sa.SA_TF32), sa.SA_ERR_UNSUPPORTED),
+    (dict(N=1000, g=list(range(300)), ng=300), sa.SA_ERR_UNSUPPORTED),
+])
+def test_host_entry_rejects_bad_arguments(lib, kwargs, status):
+    """sa_forward_host checks every argument before touching the device (this
+    runs without a GPU); host buffers need no alignment."""
+    assert _fwd_host(lib, **kwargs) == status
+    assert lib.sa_last_error().decode()
+
+
 def test_count_pairs_rejects_bad_arguments(lib):
     assert lib.sa_count_pairs(0, 8, None, 1, None, 0, None, None) == sa.SA_ERR_INVALID_ARG
     g = np.array([5], dtype=np.int32)
