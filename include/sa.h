@@ -196,7 +196,7 @@ sa_status sa_forward_global_proj(const void *q, const void *k, const void *v,
  *            gives the same result with the copies serialised on the host.
  *  out       host, [B,H,N,D] in `dtype`; fully written.
  *  lse       host, [B,H,N] float32, or NULL.
- *  heads_per_group  slices per group: 0 lets the library choose (about eight
+ *  heads_per_group  slices per group: 0 lets the library choose (about sixteen
  *            groups of at least 32 MiB of inputs each); a value below H splits
  *            each batch element's heads into groups of that many; H or more
  *            takes floor(heads_per_group / H) whole batch elements per group.

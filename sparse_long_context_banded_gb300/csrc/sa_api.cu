@@ -649,7 +649,7 @@ extern "C" sa_status sa_forward_global_proj(const void *q, const void *k, const 
 namespace sa {
 namespace {
 
-constexpr int kHostGroups = 8;                       // groups wanted per call
+constexpr int kHostGroups = 16;                      // groups wanted per call
 constexpr int64_t kHostGroupMinBytes = 32ll << 20;   // inputs of one group, at least
 
 // Batches b0 .. b0+nb-1, heads h0 .. h0+nh-1 of each (nb > 1 only with all heads).

@@ -5,8 +5,8 @@ parity tolerance (|gpu - oracle| <= 2e-3 + 1e-2 |oracle|; lse 1e-3 (1 + |oracle|
 on every row of small problems, for every way of cutting the (b, h) slices into
 groups (one head, two heads, a whole batch element, two batch elements, the
 library's choice), with pinned and with pageable host memory; and on sampled
-rows of the 131072-token workload with the library's grouping (eight groups of
-two heads), the configuration the end-to-end bench line times.  The result
+rows of the 131072-token workload with the library's grouping (sixteen groups of
+one head), the configuration the end-to-end bench line times.  The result
 must not depend on the grouping: band rows are computed by the same tiles
 whichever group holds them.
 """
