@@ -37,6 +37,11 @@
  *  - Validation happens before anything is launched; on any non-OK status
  *    nothing was enqueued and sa_last_error() describes the problem.
  *  - Thread safety: calls may come from several host threads and streams.
+ *  - Device scratch comes from one stream-ordered pool per device, created on
+ *    the first call there.  The environment variable SA_POOL_MAX_BYTES
+ *    (decimal bytes, read at that moment) caps the pool; a call whose scratch
+ *    does not fit returns SA_ERR_NO_MEMORY before any of its kernels is
+ *    launched.
  *  - Stream capture: a call may be captured into a CUDA graph once a call of
  *    the same problem (B, H, N, D, window, dilation, global set, pattern) has
  *    run on the device outside capture -- that call builds and uploads the

@@ -21,6 +21,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <atomic>
 #include <map>
@@ -51,8 +52,18 @@ sa_status fail(sa_status s, const char *fmt, ...) {
   return s;
 }
 
+// A failed runtime call also leaves its error as the thread's "last error",
+// which a later launch check (cudaGetLastError after a launch) would report as
+// its own: once recorded here, the error is consumed (a sticky error, which
+// poisons the context, stays whatever is done).
 sa_status cuda_fail(cudaError_t e, const char *what) {
+  cudaGetLastError();
   return fail(SA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+sa_status no_memory(cudaError_t e, const char *what, size_t bytes) {
+  cudaGetLastError();
+  return fail(SA_ERR_NO_MEMORY, "%s of %zu bytes: %s", what, bytes, cudaGetErrorString(e));
 }
 
 // ---------------------------------------------------------------------------
@@ -107,6 +118,12 @@ sa_status device_state(int dev, DeviceState **out) {
   props.allocType = cudaMemAllocationTypePinned;
   props.location.type = cudaMemLocationTypeDevice;
   props.location.id = dev;
+  // SA_POOL_MAX_BYTES (decimal, read once per device) caps the pool, so that
+  // the out-of-memory path can be exercised without filling the device
+  if (const char *cap = std::getenv("SA_POOL_MAX_BYTES")) {
+    const unsigned long long c = std::strtoull(cap, nullptr, 10);
+    if (c > 0) props.maxSize = (size_t)c;
+  }
   e = cudaMemPoolCreate(&ds->pool, &props);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
   uint64_t keep = ~0ull;  // keep freed scratch in the pool between calls
@@ -126,7 +143,7 @@ sa_status upload(const std::vector<X> &v, X **dst, cudaMemPool_t pool, cudaStrea
                                           stream);
   if (e != cudaSuccess) {
     *dst = nullptr;
-    return fail(SA_ERR_NO_MEMORY, "schedule buffer: %s", cudaGetErrorString(e));
+    return no_memory(e, "schedule buffer", sizeof(X) * v.size());
   }
   e = cudaMemcpyAsync(*dst, v.data(), sizeof(X) * v.size(), cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return cuda_fail(e, "copy of the schedule");
@@ -507,7 +524,7 @@ sa_status forward_impl(const void *q, const void *k, const void *v, void *out, f
   if (total > 0) {
     e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&scratch), total, ds->pool, stream);
     if (e != cudaSuccess)
-      return fail(SA_ERR_NO_MEMORY, "scratch of %zu bytes: %s", total, cudaGetErrorString(e));
+      return no_memory(e, "scratch", total);
     if (dp.g_first < 0) {
       dp.qg = scratch + off_q;
       dp.kg = scratch + off_k;
@@ -731,8 +748,7 @@ extern "C" sa_status sa_forward_host(const void *q, const void *k, const void *v
   for (int b = 0; b < 2 && result == SA_OK && b < (int)groups.size(); ++b) {
     e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&set[b]), set_bytes, ds->pool, st[0]);
     if (e != cudaSuccess)
-      result = fail(SA_ERR_NO_MEMORY, "host-call buffers of %zu bytes: %s", set_bytes,
-                    cudaGetErrorString(e));
+      result = no_memory(e, "host-call buffers", set_bytes);
   }
   for (size_t gi = 0; gi < groups.size() && result == SA_OK; ++gi) {
     const HostGroup &g = groups[gi];

@@ -88,6 +88,7 @@ sa_status static_scratch_address(int dev, char **out) {
     cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess || !ptr) {
       std::string m = std::string("cudaGetSymbolAddress(static scratch): ") + cudaGetErrorString(e);
+      cudaGetLastError();  // consumed: a later launch check must not see it
       return record_error(SA_ERR_CUDA, m.c_str());
     }
     a.ptr = static_cast<char *>(ptr);
@@ -218,6 +219,9 @@ sa_status fail_fmt(sa_status s, const char *fmt, ...) {
   va_start(ap, fmt);
   vsnprintf(buf, sizeof buf, fmt, ap);
   va_end(ap);
+  // the failed runtime call's error would otherwise linger as the thread's
+  // last error and be reported by a later launch check as its own
+  if (s == SA_ERR_CUDA) cudaGetLastError();
   return record_error(s, buf);
 }
 
