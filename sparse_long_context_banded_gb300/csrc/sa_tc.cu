@@ -1631,10 +1631,15 @@ __device__ __forceinline__ void cta_body(const Params &P, const int item0, const
         // back to the Q producer once the store has read it
         uint8_t *stage = smem + qb * C::kQBytes;
         const float inv = rcp_approx(l_run);
+        // O read out of TMEM in one load (one wait)
+        uint32_t rall[D];
+        if constexpr (D == 128)
+          tmem_ld128(t_o, rall);
+        else
+          tmem_ld64(t_o, rall);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c * 32, r);
+          const uint32_t *r = rall + 32 * c;
           // 32 output columns: a quarter of a 128-byte row chunk in bf16, a
           // whole one in fp32
           const int h = (c * 32) / C::kHalfCols;
