@@ -790,27 +790,29 @@ extern "C" sa_status sa_forward_host(const void *q, const void *k, const void *v
   // (a failure here is reported only when nothing failed before)
   for (int i = 0; i < 3; ++i)
     if (st[i]) check(cudaStreamSynchronize(st[i]), "stream synchronize");
-  for (int b = 0; b < 2; ++b)
-    if (set[b]) {
-      check(cudaFreeAsync(set[b], st[2]), "cudaFreeAsync(host-call buffers)");
-      check(cudaStreamSynchronize(st[2]), "stream synchronize");
-    }
+  int word = 0;
+  if (st[2]) {
+    for (int b = 0; b < 2; ++b)
+      if (set[b]) check(cudaFreeAsync(set[b], st[2]), "cudaFreeAsync(host-call buffers)");
+    // the device error word, read (and cleared) as sa_sync_status does, but on
+    // this call's own stream rather than the legacy default stream
+    if (result == SA_OK &&
+        check(cudaMemcpyAsync(&word, ds->err, sizeof(int), cudaMemcpyDeviceToHost, st[2]),
+              "read error word") &&
+        check(cudaStreamSynchronize(st[2]), "stream synchronize") && word != 0)
+      check(cudaMemsetAsync(ds->err, 0, sizeof(int), st[2]), "clear error word");
+    check(cudaStreamSynchronize(st[2]), "stream synchronize");
+  }
   for (int i = 0; i < 3; ++i)
     for (int b = 0; b < 2; ++b)
       if (ev[i][b]) cudaEventDestroy(ev[i][b]);
   for (int i = 0; i < 3; ++i)
     if (st[i]) cudaStreamDestroy(st[i]);
   if (result != SA_OK) return result;
-  // the device error word, as sa_sync_status reports it
-  int word = 0;
-  e = cudaMemcpy(&word, ds->err, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "read error word");
-  if (word != 0) {
-    cudaMemset(ds->err, 0, sizeof(int));
-    if (word & kErrWaitTimeout)
-      return fail(SA_ERR_TIMEOUT, "a kernel gave up on a stalled wait (error word 0x%x)", word);
+  if (word & kErrWaitTimeout)
+    return fail(SA_ERR_TIMEOUT, "a kernel gave up on a stalled wait (error word 0x%x)", word);
+  if (word != 0)
     return fail(SA_ERR_CUDA, "a kernel failed a device-side check (error word 0x%x)", word);
-  }
   return SA_OK;
 }
 
