@@ -60,6 +60,27 @@ def test_host_entry_every_row(case, heads_per_group, oracle):
     assert_lse_close(got_lse, ref_lse, what)
 
 
+EDGE_CASES = [
+    # B, H, N, D, window, dilation, globals, dtype, tf32
+    (1, 1, 1, 64, 16, [1], [0], "bf16", False),          # one row, one head
+    (1, 1, 129, 128, 0, [1], [], "bf16", False),         # no window, no globals
+    (1, 2, 700, 64, 128, [1, 2], [0, 699], "fp32", True),  # fp32 inputs on the tensor cores (tf32)
+]
+
+
+@pytest.mark.parametrize("case", EDGE_CASES, ids=lambda c: "B{}H{}N{}D{}-{}{}".format(
+    *c[:4], c[7], "-tf32" if c[8] else ""))
+def test_host_entry_edge_cases(case, oracle):
+    import torch
+    B, H, N, D, window, dil, G, dtype, tf32 = case
+    w = inputs.custom(B, H, N, D, window, dilation=dil, globals_=G, dtype=dtype)
+    q, k, v = inputs.draw_qkv(w, seed=44)
+    hq, hk, hv = (host(a, torch, True) for a in (q, k, v))
+    out = sa.forward_host(hq, hk, hv, window, dil, G, tf32=tf32)  # no lse
+    ref, _ = oracle.forward_longformer(q, k, v, window, dil, G, scale=D ** -0.5, want_lse=False)
+    assert_close(out.float().numpy().astype(np.float64), ref, f"host entry {case}")
+
+
 def test_host_entry_pageable_matches_pinned():
     B, H, N, D = 2, 4, 1200, 64
     w = inputs.custom(B, H, N, D, 256, dilation=[1, 2, 1, 3], globals_=[0, 600], dtype="bf16")
@@ -86,6 +107,9 @@ def test_host_entry_rejects_device_tensors():
     q = torch.zeros(1, 1, 64, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError):
         sa.forward_host(q, q, q, 8)
+    h = torch.zeros(1, 1, 64, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        sa.forward_host(h, h, h, 8, out=q)
 
 
 def test_host_entry_long_context_sampled(oracle):
